@@ -1,0 +1,10 @@
+"""CPU oracle for exact attention (test infrastructure only; see attention.py)."""
+from .attention import (  # noqa: F401
+    attention,
+    attention_rows,
+    bf16_round,
+    flash_fa1,
+    flash_fa2,
+    naive_bf16_attention,
+    safe_softmax,
+)
