@@ -1,0 +1,416 @@
+"""Benchmark of the fused exact-attention forward pass.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference] [--workload NAME]
+
+One step = one call of fa_fwd over the whole workload (every (b, h) and
+query row). The default workload is the 8k-context prefill shape
+(B=1, H=32, N=8192, d=128, bf16, seeded synthetic inputs). Metric: forward
+TFLOP/s counted as 4*B*H*N^2*d / time. Rank 0 prints one JSON line.
+
+Timing: W untimed warm-up steps; then K steps, each bracketed by CUDA events
+on the launching stream, with the L2 cache flushed (a 512 MB write) before
+every step, outside the events; barrier + synchronize around the timed
+region; the max over ranks of the summed device time. For N > 1 (launched by
+torchrun) every rank runs its own copy of the workload (independent problems,
+no collective on the data path): weak scaling.
+
+--impl reference times the CPU oracle (float64, numpy) on the host cores, on a
+bounded sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s (4·B·H·N²·d) and % of GB300 dense BF16 peak, 1 GPU"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "prefill8k_d128_h32"
+KERNEL_NAME = "fa_fwd_kernel<128>"
+KERNEL_SOURCES = ["exact_io_aware_34_gb300/csrc/fa_api.cu", "exact_io_aware_34_gb300/csrc/fa_fwd_kernel.cuh",
+                  "exact_io_aware_34_gb300/csrc/sm103a_ptx.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+# ----------------------------------------------------------------------------- helpers
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in ("bf16_tflops", "bf16_tflops_sustained", "hbm_gbs")}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    current kernel sources; otherwise None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = t.get(workload)
+    if not entry or entry.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+        return False
+
+    def summary(self):
+        rows = [r.split(", ") for r in (self.out or "").strip().splitlines() if r.strip()]
+        rows = [r for r in rows if len(r) == len(self.FIELDS)]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "", 1).isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "", 1).isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        power = [float(r[3]) for r in rows if r[3].replace(".", "", 1).isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max of a float over all ranks (identity when world == 1)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+def _oracle_rows_worker(args):
+    """Pool task: oracle.attention_rows on the given (b, h, r) rows; returns seconds."""
+    import numpy as np
+    import oracle as _oracle
+    name, rows = args
+    Q, K, V, s = _cached_inputs(name)
+    t0 = time.perf_counter()
+    _oracle.attention_rows(Q, K, V, s, np.asarray(rows))
+    return time.perf_counter() - t0
+
+
+_INPUT_CACHE = {}
+
+
+def _cached_inputs(name):
+    """The workload's inputs as float32 numpy arrays, generated once per process."""
+    from exact_io_aware_34_gb300 import inputs as _inp
+    if name not in _INPUT_CACHE:
+        q, k, v, s = _inp.make_inputs(_inp.workload(name))
+        _INPUT_CACHE[name] = (q.float().numpy(), k.float().numpy(), v.float().numpy(), s)
+    return _INPUT_CACHE[name]
+
+
+def _worker_init(name, ready):
+    _cached_inputs(name)
+    ready.wait()
+
+
+def _noop(_):
+    return 0
+
+
+class OracleTimer:
+    """Times the CPU oracle on row samples of a workload, in a pool of spawned
+    single-threaded worker processes (one per host core). Every worker builds
+    its copy of the inputs before the first timed task."""
+
+    def __init__(self, name: str, cores: int | None = None):
+        import multiprocessing as mp
+        from exact_io_aware_34_gb300 import inputs as _inp
+        self.name = name
+        self.w = _inp.workload(name)
+        self.cores = cores or len(os.sched_getaffinity(0))
+        os.environ["OPENBLAS_NUM_THREADS"] = "1"
+        os.environ["OMP_NUM_THREADS"] = "1"
+        ctx = mp.get_context("spawn")
+        ready = ctx.Barrier(self.cores)
+        self.pool = ctx.Pool(self.cores, initializer=_worker_init, initargs=(name, ready))
+        self.pool.map(_noop, range(4 * self.cores), chunksize=1)
+
+    def run(self, n_rows: int, seed: int = 0):
+        """Oracle rows (b, h, r) spread over the workload; returns (wall seconds, flops)."""
+        import numpy as np
+        w = self.w
+        rng = np.random.default_rng(seed)
+        flat = rng.choice(w.B * w.H * w.N, size=min(n_rows, w.B * w.H * w.N), replace=False)
+        rows = np.stack([flat // (w.H * w.N), (flat // w.N) % w.H, flat % w.N], axis=1)
+        # group rows by head so each task converts one head's K and V once
+        order = np.lexsort((rows[:, 2], rows[:, 1], rows[:, 0]))
+        rows = rows[order]
+        chunks = [c.tolist() for c in np.array_split(rows, self.cores) if len(c)]
+        t0 = time.perf_counter()
+        self.pool.map(_oracle_rows_worker, [(self.name, c) for c in chunks])
+        dt = time.perf_counter() - t0
+        return dt, 4.0 * len(rows) * w.N * w.d
+
+    def calibrate(self, target_s: float) -> int:
+        """Rows per sample so that one sample takes about ``target_s`` seconds."""
+        total = self.w.B * self.w.H * self.w.N
+        n = 4 * self.cores
+        while True:
+            dt, _ = self.run(n, seed=99)
+            if dt >= 0.2 * target_s or n >= total:
+                break
+            n = min(total, n * 4)
+        rows = int(n * target_s / max(dt, 1e-4))
+        return max(self.cores, min(rows, total))
+
+    def close(self):
+        self.pool.terminate()
+        self.pool.join()
+
+
+def cpu_baseline(name: str, target_s: float = 15.0):
+    t = OracleTimer(name)
+    try:
+        rows = t.calibrate(target_s)
+        dt, flops = t.run(rows, seed=1)
+    finally:
+        t.close()
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": t.cores, "kind": "oracle",
+            "sample": f"{rows} query rows drawn uniformly from the {name} workload (all {t.w.N} keys each), "
+                      f"float64 numpy oracle, {t.cores} single-threaded worker processes, {dt:.1f} s"}
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    from exact_io_aware_34_gb300 import inputs
+    w = inputs.workload(args.workload)
+    t = OracleTimer(args.workload)
+    try:
+        rows = t.calibrate(args.ref_step_s)
+        for i in range(args.warmup):
+            t.run(rows, seed=1000 + i)
+        times, flops = [], 0.0
+        for i in range(args.steps):
+            dt, f = t.run(rows, seed=i)
+            times.append(dt)
+            flops += f
+    finally:
+        t.close()
+    total = sum(times)
+    value = flops / total / 1e12
+    sample = (f"each step: {rows} query rows drawn uniformly from the {w.name} workload (all {w.N} keys each), "
+              f"float64 numpy oracle, {t.cores} single-threaded worker processes")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded, bf16-rounded inputs)",
+        "config": {**w.describe(), "workload": w.name, "sample_rows_per_step": rows},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": t.cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- native arm
+def run_native(args):
+    import torch
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+
+    # The CPU baseline runs before the first GPU call (its worker pool is spawned).
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.workload, target_s=args.cpu_seconds)
+
+    from exact_io_aware_34_gb300 import build as fa_build
+    from exact_io_aware_34_gb300 import fa, inputs
+    fa_build.build()
+    fa.load_library()
+    w = inputs.workload(args.workload)
+    q, k, v, scale = inputs.make_inputs(w)
+    B, H, N, d = q.shape
+    flops = w.flops
+    qd, kd, vd = (x.to(device) for x in (q, k, v))
+    o = torch.empty_like(qd)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    for _ in range(args.warmup):
+        fa.fa_fwd(qd, kd, vd, o, lse, scale)
+    torch.cuda.synchronize(device)
+    st, info = fa.fa_get_device_status()
+    if st != fa.FA_OK:
+        raise RuntimeError(f"device status after warm-up: {fa.fa_status_string(st)} {info}")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    with ClockSampler(local) as clocks:
+        time.sleep(0.3)
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            starts[i].record(stream)
+            fa.fa_fwd(qd, kd, vd, o, lse, scale)
+            ends[i].record(stream)
+        torch.cuda.synchronize(device)
+    barrier(world, device)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = reduce_max(sum(step_ms), world, device)
+    st, info = fa.fa_get_device_status()
+    if st != fa.FA_OK:
+        raise RuntimeError(f"device status after timed steps: {fa.fa_status_string(st)} {info}")
+
+    # end to end through the public API: pinned host inputs in, O and LSE back out
+    qh, kh, vh = (x.pin_memory() for x in (q, k, v))
+    oh = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    lh = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 10))
+    for i in range(2):
+        qd.copy_(qh, non_blocking=True); kd.copy_(kh, non_blocking=True); vd.copy_(vh, non_blocking=True)
+        fa.fa_fwd(qd, kd, vd, o, lse, scale)
+        oh.copy_(o, non_blocking=True); lh.copy_(lse, non_blocking=True)
+    torch.cuda.synchronize(device)
+    barrier(world, device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e2e_steps):
+        qd.copy_(qh, non_blocking=True); kd.copy_(kh, non_blocking=True); vd.copy_(vh, non_blocking=True)
+        fa.fa_fwd(qd, kd, vd, o, lse, scale)
+        oh.copy_(o, non_blocking=True); lh.copy_(lse, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = reduce_max(e0.elapsed_time(e1), world, device)
+    h2d = 3 * q.numel() * 2
+    d2h = o.numel() * 2 + lse.numel() * 4
+
+    if rank == 0:
+        peaks, peak_src = load_peaks()
+        avg_ms = sum(step_ms) / len(step_ms)
+        achieved = flops / (avg_ms * 1e-3) / 1e12
+        value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+        traffic = load_traffic(w.name)
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; Q,K ~ N(0,1), V ~ U(-1,1), bf16)",
+            "config": {**w.describe(), "l2": "flushed before every step (512 MB write, outside the events)",
+                       "parallelism": f"replicas x{world} (independent problems per rank)"},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": UNIT,
+                         "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
+                         "peak_source": f"{peak_src} dense bf16 burst",
+                         "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                         "kernel": KERNEL_NAME, "flops_per_launch": flops,
+                         "algorithmic_bytes_per_launch": B * H * N * (8 * d + 4)},
+            "e2e": {"value": world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps,
+            "clocks": clocks.summary(),
+            "step_ms": {"min": min(step_ms), "median": statistics.median(step_ms), "max": max(step_ms)},
+        }
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU oracle sample size (seconds of work)")
+    ap.add_argument("--ref-step-s", type=float, default=2.0, help="reference arm: seconds of oracle work per step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_native(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,179 @@
+// C ABI of the exact attention forward pass (declared in include/fa.h):
+// argument checks, TMA descriptor encoding, the launch on the caller's
+// stream, and the device status word.
+//
+// One launch per call ("01 · 注意力为什么是 IO 瓶颈" §6: the fused forward is a
+// single kernel launch on the caller's stream). Unlike the upstream library
+// described there, which allocates softmax_lse itself, the caller owns O and
+// LSE here and this file allocates no device memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_fwd_kernel.cuh"
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+
+fa_status_t cuda_fail(cudaError_t e) {
+  t_last_cuda_error = static_cast<int>(e);
+  return FA_ERR_CUDA;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// [B*H, N, d] bf16 view of a contiguous [B, H, N, d] tensor; box = 64 x 128
+// rows x 1 head, 128-byte swizzle. Rows beyond N of a head are outside the
+// tensor and read as zeros, so a ragged last block never sees the next head.
+bool make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  auto x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+template <int HD>
+fa_status_t launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N,
+                   float scale, int drop_load, unsigned long long timeout_ns, cudaStream_t stream) {
+  using C = fa::FwdCfg<HD>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  // The dynamic shared-memory opt-in is per function and device context.
+  static std::once_flag attr_once[64];
+  static cudaError_t attr_err[64];
+  if (dev < 0 || dev >= 64) return FA_ERR_UNSUPPORTED;
+  std::call_once(attr_once[dev], [&] {
+    attr_err[dev] = cudaFuncSetAttribute(fa::fa_fwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+  });
+  if (attr_err[dev] != cudaSuccess) return cuda_fail(attr_err[dev]);
+
+  CUtensorMap mq, mk, mv;
+  const int BH = B * H;
+  if (!make_map(&mq, Q, BH, N, HD) || !make_map(&mk, K, BH, N, HD) || !make_map(&mv, V, BH, N, HD))
+    return cuda_fail(cudaErrorInvalidValue);
+
+  fa::FwdParams p;
+  p.O = static_cast<__nv_bfloat16*>(O);
+  p.LSE = LSE;
+  p.N = N;
+  p.H = H;
+  p.n_kv_blocks = (N + C::kBN - 1) / C::kBN;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  p.timeout_ns = timeout_ns;
+  p.drop_load = drop_load;
+
+  dim3 grid((N + C::kQTiles * C::kBM - 1) / (C::kQTiles * C::kBM), H, B);
+  fa::fa_fwd_kernel<HD><<<grid, C::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FA_OK;
+}
+
+fa_status_t fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
+                     float scale, int drop_load, unsigned long long timeout_ns, cudaStream_t stream) {
+  if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+  if (B > 65535 || H > 65535) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H * N >= (1LL << 31)) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (scale < 0.f) return FA_ERR_UNSUPPORTED;
+  for (const void* ptr : {Q, K, V, static_cast<const void*>(O)})
+    if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return FA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(LSE) % 4 != 0) return FA_ERR_INVALID_ARG;
+  const size_t n_qkv = static_cast<size_t>(B) * H * N * d * 2;
+  const size_t n_lse = static_cast<size_t>(B) * H * N * 4;
+  for (const void* in : {Q, K, V}) {
+    if (overlaps(O, n_qkv, in, n_qkv) || overlaps(LSE, n_lse, in, n_qkv)) return FA_ERR_INVALID_ARG;
+  }
+  if (overlaps(O, n_qkv, LSE, n_lse)) return FA_ERR_INVALID_ARG;
+  if (d == 64) return launch<64>(Q, K, V, O, LSE, B, H, N, scale, drop_load, timeout_ns, stream);
+  return launch<128>(Q, K, V, O, LSE, B, H, N, scale, drop_load, timeout_ns, stream);
+}
+
+// A correct pipeline never waits anywhere near this long; it only bounds
+// how long a broken one can hold the GPU.
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
+
+}  // namespace
+
+extern "C" {
+
+fa_status_t fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
+                   float scale, cudaStream_t stream) {
+  return fwd_impl(Q, K, V, O, LSE, B, H, N, d, scale, -1, kDefaultTimeoutNs, stream);
+}
+
+fa_status_t fa_fwd_fault_test(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+                              int N, int d, float scale, int drop_load, unsigned long long timeout_ns,
+                              cudaStream_t stream) {
+  if (timeout_ns == 0) return FA_ERR_INVALID_ARG;
+  return fwd_impl(Q, K, V, O, LSE, B, H, N, d, scale, drop_load < 0 ? -1 : drop_load, timeout_ns, stream);
+}
+
+fa_status_t fa_get_device_status(cudaStream_t stream, unsigned int* info) {
+  if (info)
+    for (int i = 0; i < 4; ++i) info[i] = 0;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  unsigned int word = 0;
+  e = cudaMemcpyFromSymbol(&word, fa::g_status_word, sizeof(word));
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (word == 0) return FA_OK;
+  unsigned int details[4] = {0, 0, 0, 0};
+  e = cudaMemcpyFromSymbol(details, fa::g_status_info, sizeof(details));
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (info)
+    for (int i = 0; i < 4; ++i) info[i] = details[i];
+  const unsigned int zeros[4] = {0, 0, 0, 0};
+  e = cudaMemcpyToSymbol(fa::g_status_word, zeros, sizeof(unsigned int));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(fa::g_status_info, zeros, sizeof(zeros));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FA_ERR_TIMEOUT;
+}
+
+const char* fa_status_string(fa_status_t status) {
+  switch (status) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+  }
+  return "FA_ERR_UNKNOWN";
+}
+
+int fa_last_cuda_error(void) { return t_last_cuda_error; }
+
+}  // extern "C"

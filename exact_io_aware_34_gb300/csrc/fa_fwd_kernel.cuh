@@ -1,0 +1,455 @@
+// Fused exact-attention forward kernel for sm_103a (tcgen05 + TMEM + TMA).
+//
+// One CTA owns 2 query tiles of 128 rows (256 query rows) of one (b, h) and
+// streams every 128-row key/value block of that head past them:
+//   "Flash Attention (FA1)", "Tiling in FlashAttention": Q in Br x d blocks,
+//   K and V in Bc x d blocks, Tc = ceil(N / Bc); here Br = Bc = 128 (the
+//   tcgen05 M and the key-block width). The CTA runs the query-outer order
+//   ("01 · 注意力为什么是 IO 瓶颈" §5 skeleton; the FlashAttention-2 split of
+//   "FlashAttention：IO 感知的精确注意力", core concepts).
+//
+// Per key block j and query tile t the update is the page's online softmax
+// ("Flash Attention (FA1)", derivation steps 1-5) in its unnormalised form:
+//   S = Q_t K_j^T                        (tcgen05.mma, fp32 in TMEM)
+//   m_new = max(m, rowmax(S))            (step 2)
+//   P = exp(scale*(S - m_new))           (step 1 taken against m_new)
+//   l = l * e^{scale(m - m_new)} + rowsum(P)      (step 2)
+//   O = O * e^{scale(m - m_new)} + P V_j          (steps 3-5, numerator form)
+// and after the last block O /= l, LSE = scale*m + ln l.
+//
+// Exactness-preserving deviation: the running maximum used for the
+// exponentials is only moved when the new row maximum exceeds it by more
+// than kRescaleLog2 (in log2 units of the scaled score). Until then the
+// stale maximum keeps serving both l and O, so every term of O and l carries
+// the same factor and O / l and (m + ln l) are unchanged; the probabilities
+// stay below 2^kRescaleLog2, far inside bf16/fp32 range. This skips most of
+// the O rescales (a TMEM read-modify-write of 128 x d floats).
+//
+// Warp roles (10 warps):
+//   warps 0-3  softmax + epilogue for query tile 0 (one thread per row)
+//   warps 4-7  softmax + epilogue for query tile 1
+//   warp 8     TMA producer (one thread)
+//   warp 9     TMEM allocator and MMA issuer (one thread issues)
+// TMEM (512 columns x 128 lanes x 32 bit): S_t at column 128*t (P_t, packed
+// bf16, overwrites the first 64 of those columns), O_t at 256 + d*t.
+// Shared memory: Q tiles (2 x 128 x d bf16) + a ring of K/V tiles
+// (kStages x 128 x d bf16), each tile stored as d/64 chunks of 128 rows x
+// 128 bytes in the 128-byte swizzled layout that TMA writes and the tensor
+// core reads.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "sm103a_ptx.cuh"
+
+namespace fa {
+
+// Device status word (set on a wait timeout) and the first timeout's details.
+// Read and cleared by fa_get_device_status().
+__device__ unsigned int g_status_word;
+__device__ unsigned int g_status_info[4];
+
+enum : unsigned int { kRoleProducer = 1, kRoleMma = 2, kRoleSoftmax = 3 };
+
+template <int HD>
+struct FwdCfg {
+  static constexpr int kBM = 128;        // query rows per tile (tcgen05 M)
+  static constexpr int kBN = 128;        // keys per K/V block
+  static constexpr int kQTiles = 2;      // query tiles per CTA
+  static constexpr int kChunks = HD / 64;          // 128-byte swizzle chunks per row
+  static constexpr int kChunkBytes = 128 * 128;    // 128 rows x 128 bytes
+  static constexpr int kTileBytes = kChunks * kChunkBytes;   // one Q, K or V tile
+  static constexpr int kStages = (HD == 128) ? 4 : 8;        // K/V ring slots
+  static constexpr int kSmemQ = kQTiles * kTileBytes;
+  static constexpr int kSmemKV = kStages * kTileBytes;
+  static constexpr int kSmemBytes = kSmemQ + kSmemKV + 1024;  // + alignment slack
+  static constexpr int kThreads = 320;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColS = 0;         // + 128 * t
+  static constexpr uint32_t kColO = 256;       // + HD * t
+  static constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(kBM, kBN, false, false);
+  static constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kBM, HD, false, true);
+};
+
+struct FwdParams {
+  __nv_bfloat16* O;
+  float* LSE;
+  int N;
+  int H;
+  int n_kv_blocks;
+  float scale_log2;            // scale * log2(e)
+  unsigned long long timeout_ns;
+  int drop_load;               // test hook: index of a K/V load to skip, -1 = none
+};
+
+constexpr float kRescaleLog2 = 8.0f;
+
+// Bounded wait. Returns false when the CTA is aborting (another role gave up)
+// or when this wait itself ran out of time, in which case it raises the abort
+// flag and records the timeout in the device status word.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                              unsigned long long timeout_ns, unsigned int role) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (ptx::globaltimer_ns() - t0 > timeout_ns) {
+      *abort_flag = 1;
+      if (atomicCAS(&g_status_word, 0u, 1u) == 0u) {
+        g_status_info[0] = role;
+        g_status_info[1] = blockIdx.x;
+        g_status_info[2] = blockIdx.y;
+        g_status_info[3] = blockIdx.z;
+      }
+      __threadfence();
+      return false;
+    }
+  }
+}
+
+// Warp-uniform bounded wait for the 32 lanes of a softmax warp: returns the
+// same answer in every lane, so the warp-collective TMEM instructions that
+// follow are never reached by part of a warp.
+__device__ __forceinline__ bool wait_warp_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                   unsigned long long timeout_ns, unsigned int role) {
+  if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  const int lane = threadIdx.x & 31;
+  while (true) {
+    if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
+    int stop = 0;
+    if (lane == 0) {
+      if (*abort_flag) {
+        stop = 1;
+      } else if (ptx::globaltimer_ns() - t0 > timeout_ns) {
+        *abort_flag = 1;
+        if (atomicCAS(&g_status_word, 0u, 1u) == 0u) {
+          g_status_info[0] = role;
+          g_status_info[1] = blockIdx.x;
+          g_status_info[2] = blockIdx.y;
+          g_status_info[3] = blockIdx.z;
+        }
+        __threadfence();
+        stop = 1;
+      }
+    }
+    if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+  }
+}
+
+// Bounded wait used only while cleaning up after an abort: ignores the abort
+// flag, gives up silently after `timeout_ns`.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsigned long long timeout_ns) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer_ns() - t0 > timeout_ns) return;
+  }
+}
+
+template <int HD>
+__global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  using C = FwdCfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_q_full;
+  __shared__ __align__(8) uint64_t bar_kv_full[C::kStages];
+  __shared__ __align__(8) uint64_t bar_kv_empty[C::kStages];
+  __shared__ __align__(8) uint64_t bar_s_full[2];
+  __shared__ __align__(8) uint64_t bar_p_full[2];
+  __shared__ __align__(8) uint64_t bar_o_full[2];
+  __shared__ __align__(8) uint64_t bar_drain;
+  __shared__ uint32_t tmem_base_slot;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bh = blockIdx.z * p.H + blockIdx.y;
+  const int q_row0 = blockIdx.x * (C::kQTiles * C::kBM);
+  const int n_kv = p.n_kv_blocks;
+
+  // 1024-byte aligned base: the 128-byte swizzle pattern is a function of
+  // the shared-memory address bits [4, 10).
+  const uint32_t smem_base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sQ = smem_base;
+  const uint32_t sKV = smem_base + C::kSmemQ;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_u32(&bar_q_full), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&bar_kv_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bar_kv_empty[s]), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      ptx::mbar_init(ptx::smem_u32(&bar_s_full[t]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bar_p_full[t]), C::kBM);
+      ptx::mbar_init(ptx::smem_u32(&bar_o_full[t]), 1);
+    }
+    ptx::mbar_init(ptx::smem_u32(&bar_drain), 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 9) {
+    ptx::tmem_alloc(ptx::smem_u32(&tmem_base_slot), C::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (warp == 8 && lane == 0) {
+    ptx::prefetch_tmap(&tmQ);
+    ptx::prefetch_tmap(&tmK);
+    ptx::prefetch_tmap(&tmV);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = tmem_base_slot;
+  volatile int* abort_ptr = &abort_flag;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_q = ptx::policy_evict_first();
+      const uint64_t pol_kv = ptx::policy_evict_last();
+      const uint32_t q_full = ptx::smem_u32(&bar_q_full);
+      ptx::mbar_arrive_expect_tx(q_full, C::kQTiles * C::kTileBytes);
+      for (int t = 0; t < C::kQTiles; ++t)
+        for (int c = 0; c < C::kChunks; ++c)
+          ptx::tma_load_3d(sQ + t * C::kTileBytes + c * C::kChunkBytes, &tmQ, q_full, c * 64,
+                           q_row0 + t * C::kBM, bh, pol_q);
+      int issued = 0;
+      bool ok = true;
+      for (int j = 0; j < n_kv && ok; ++j) {
+        for (int kv = 0; kv < 2; ++kv) {
+          const int it = 2 * j + kv;
+          const int slot = it % C::kStages;
+          const uint32_t phase = (it / C::kStages) & 1;
+          if (!wait_or_abort(ptx::smem_u32(&bar_kv_empty[slot]), phase ^ 1u, abort_ptr, p.timeout_ns,
+                             kRoleProducer)) {
+            ok = false;
+            break;
+          }
+          issued = it + 1;
+          if (it == p.drop_load) continue;   // test hook: this tile never arrives
+          const uint32_t full = ptx::smem_u32(&bar_kv_full[slot]);
+          ptx::mbar_arrive_expect_tx(full, C::kTileBytes);
+          const void* map = kv ? static_cast<const void*>(&tmV) : static_cast<const void*>(&tmK);
+          for (int c = 0; c < C::kChunks; ++c)
+            ptx::tma_load_3d(sKV + slot * C::kTileBytes + c * C::kChunkBytes, map, full, c * 64,
+                             j * C::kBN, bh, pol_kv);
+        }
+      }
+      if (!ok || *abort_ptr) {
+        // Let every copy this thread started land before the CTA exits.
+        drain_wait(q_full, 0, p.timeout_ns);
+        const int first = issued > C::kStages ? issued - C::kStages : 0;
+        for (int it = first; it < issued; ++it) {
+          if (it == p.drop_load) continue;
+          drain_wait(ptx::smem_u32(&bar_kv_full[it % C::kStages]), (it / C::kStages) & 1, p.timeout_ns);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = wait_or_abort(ptx::smem_u32(&bar_q_full), 0, abort_ptr, p.timeout_ns, kRoleMma);
+      ptx::tc_fence_after();
+      // P V for query tile t and key block jj (P_t sits in the S_t columns).
+      auto issue_pv = [&](int t, int jj) {
+        const int it = 2 * jj + 1;
+        const uint32_t v_tile = sKV + (it % C::kStages) * C::kTileBytes;
+        const uint32_t d_tmem = tmem_base + C::kColO + HD * t;
+        const uint32_t a_tmem = tmem_base + C::kColS + 128 * t;
+#pragma unroll
+        for (int kk = 0; kk < C::kBN / 16; ++kk) {
+          const uint64_t b_desc = ptx::desc_mnmajor_sw128(v_tile + kk * 16 * 128, C::kChunkBytes);
+          ptx::mma_ts(d_tmem, a_tmem + kk * 8, b_desc, C::kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
+        }
+      };
+      // S_t = Q_t K_j^T.
+      auto issue_qk = [&](int t, int j) {
+        const int it = 2 * j;
+        const uint32_t k_tile = sKV + (it % C::kStages) * C::kTileBytes;
+        const uint32_t q_tile = sQ + t * C::kTileBytes;
+        const uint32_t d_tmem = tmem_base + C::kColS + 128 * t;
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+          ptx::mma_ss(d_tmem, ptx::desc_kmajor_sw128(q_tile + off), ptx::desc_kmajor_sw128(k_tile + off),
+                      C::kIdescQK, kk > 0 ? 1u : 0u);
+        }
+      };
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int itK = 2 * j;
+        ok = wait_or_abort(ptx::smem_u32(&bar_kv_full[itK % C::kStages]), (itK / C::kStages) & 1, abort_ptr,
+                           p.timeout_ns, kRoleMma);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j > 0) {
+            ok = wait_or_abort(ptx::smem_u32(&bar_p_full[t]), (j - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
+            if (!ok) break;
+            if (t == 0) {
+              const int itV = 2 * (j - 1) + 1;
+              ok = wait_or_abort(ptx::smem_u32(&bar_kv_full[itV % C::kStages]), (itV / C::kStages) & 1,
+                                 abort_ptr, p.timeout_ns, kRoleMma);
+              if (!ok) break;
+            }
+            ptx::tc_fence_after();
+            issue_pv(t, j - 1);
+            if (t == 1) ptx::mma_commit(ptx::smem_u32(&bar_kv_empty[(2 * (j - 1) + 1) % C::kStages]));
+          }
+          issue_qk(t, j);
+          ptx::mma_commit(ptx::smem_u32(&bar_s_full[t]));
+        }
+        if (ok) ptx::mma_commit(ptx::smem_u32(&bar_kv_empty[itK % C::kStages]));
+      }
+      // The last key block's P V.
+      for (int t = 0; t < 2 && ok; ++t) {
+        ok = wait_or_abort(ptx::smem_u32(&bar_p_full[t]), (n_kv - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
+        if (!ok) break;
+        if (t == 0) {
+          const int itV = 2 * (n_kv - 1) + 1;
+          ok = wait_or_abort(ptx::smem_u32(&bar_kv_full[itV % C::kStages]), (itV / C::kStages) & 1, abort_ptr,
+                             p.timeout_ns, kRoleMma);
+          if (!ok) break;
+        }
+        ptx::tc_fence_after();
+        issue_pv(t, n_kv - 1);
+        ptx::mma_commit(ptx::smem_u32(&bar_o_full[t]));
+        if (t == 1) ptx::mma_commit(ptx::smem_u32(&bar_kv_empty[(2 * (n_kv - 1) + 1) % C::kStages]));
+      }
+      if (!ok) {
+        // Wait for every MMA already issued before TMEM is freed.
+        ptx::mma_commit(ptx::smem_u32(&bar_drain));
+        drain_wait(ptx::smem_u32(&bar_drain), 0, p.timeout_ns);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int t = warp >> 2;                 // query tile
+    const int quarter = warp & 3;            // TMEM lane quarter
+    const int row = quarter * 32 + lane;     // row within the tile
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem_base + lane_addr + C::kColS + 128 * t;
+    const uint32_t tO = tmem_base + lane_addr + C::kColO + HD * t;
+    const float sl2 = p.scale_log2;
+    float m_use = 0.f;      // raw-score maximum the exponentials are taken against
+    float l = 0.f;          // running sum of exp, relative to m_use
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      ok = wait_warp_or_abort(ptx::smem_u32(&bar_s_full[t]), j & 1, abort_ptr, p.timeout_ns, kRoleSoftmax);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      uint32_t s[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + 32 * c, s[c]);
+      ptx::tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) ptx::reg_fence32(s[c]);
+
+      const int valid = p.N - j * C::kBN;    // keys of this block that exist
+      if (valid < C::kBN) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (32 * c + i >= valid) s[c][i] = __float_as_uint(-INFINITY);
+      }
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) mt = fmaxf(mt, __uint_as_float(s[c][i]));
+
+      float alpha = 1.f;
+      bool rescale_o = false;
+      if (j == 0) {
+        m_use = mt;
+      } else {
+        const bool need = (mt - m_use) * sl2 > kRescaleLog2;
+        rescale_o = __any_sync(0xffffffffu, need);
+        if (need) {
+          alpha = ptx::ex2_approx((m_use - mt) * sl2);
+          m_use = mt;
+        }
+      }
+      const float neg_m = -m_use * sl2;
+      float sum = 0.f;
+      uint32_t pk[2][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          float p0 = ptx::ex2_approx(fmaf(__uint_as_float(s[c][i]), sl2, neg_m));
+          float p1 = ptx::ex2_approx(fmaf(__uint_as_float(s[c][i + 1]), sl2, neg_m));
+          if (valid < C::kBN) {
+            if (32 * c + i >= valid) p0 = 0.f;
+            if (32 * c + i + 1 >= valid) p1 = 0.f;
+          }
+          sum += p0 + p1;
+          pk[c >> 1][(c & 1) * 16 + (i >> 1)] = ptx::pack_bf16x2(p0, p1);
+        }
+      }
+      l = l * alpha + sum;
+      ptx::tmem_st32(tS, pk[0]);
+      ptx::tmem_st32(tS + 32, pk[1]);
+      if (rescale_o) {
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t o[32];
+          ptx::tmem_ld32(tO + 32 * c, o);
+          ptx::tmem_ld_wait();
+          ptx::reg_fence32(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          ptx::tmem_st32(tO + 32 * c, o);
+        }
+      }
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(ptx::smem_u32(&bar_p_full[t]));
+    }
+    if (ok) ok = wait_warp_or_abort(ptx::smem_u32(&bar_o_full[t]), 0, abort_ptr, p.timeout_ns, kRoleSoftmax);
+    if (ok) {
+      ptx::tc_fence_after();
+      const int grow = q_row0 + t * C::kBM + row;
+      const bool in_range = grow < p.N;
+      const float inv_l = 1.f / l;
+      __nv_bfloat16* orow = p.O + (static_cast<size_t>(bh) * p.N + grow) * HD;
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t o[32];
+        ptx::tmem_ld32(tO + 32 * c, o);
+        ptx::tmem_ld_wait();
+        ptx::reg_fence32(o);
+        uint32_t packed[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          packed[i] = ptx::pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+        if (in_range) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+        }
+      }
+      if (in_range) {
+        // LSE = scale * m + ln l = (scale*log2(e) * m + log2 l) * ln 2
+        p.LSE[static_cast<size_t>(bh) * p.N + grow] = (m_use * sl2 + __log2f(l)) * 0.69314718055994530942f;
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+}  // namespace fa

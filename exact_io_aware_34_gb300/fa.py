@@ -1,0 +1,145 @@
+"""Thin Python binding of the C ABI in include/fa.h (argument marshalling only).
+
+Every step of the attention forward pass runs in the CUDA library
+``libfa.so``; this module only checks tensor metadata, passes raw device
+pointers and the current CUDA stream, and turns status codes into
+exceptions. There is no fallback: if the library is missing, every call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfa.so")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_CUDA = 3
+FA_ERR_TIMEOUT = 4
+
+#: every symbol include/fa.h declares
+EXPORTED = ("fa_fwd", "fa_get_device_status", "fa_status_string", "fa_last_cuda_error", "fa_fwd_fault_test")
+
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = f"{where}: {fa_status_string(status)}"
+        if status == FA_ERR_CUDA:
+            msg += f" (cudaError {fa_last_cuda_error()})"
+        super().__init__(msg)
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libfa.so (once). Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with exact_io_aware_34_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    vp, i, f, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_ulonglong
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, vp]
+    lib.fa_fwd.restype = i
+    lib.fa_fwd_fault_test.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, u64, vp]
+    lib.fa_fwd_fault_test.restype = i
+    lib.fa_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
+    lib.fa_get_device_status.restype = i
+    lib.fa_status_string.argtypes = [i]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_last_cuda_error.argtypes = []
+    lib.fa_last_cuda_error.restype = i
+    _lib = lib
+    return lib
+
+
+def fa_status_string(status: int) -> str:
+    return load_library().fa_status_string(int(status)).decode()
+
+
+def fa_last_cuda_error() -> int:
+    return int(load_library().fa_last_cuda_error())
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check_qkv(q, k, v):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be bfloat16, got {t.dtype}")
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be [B, H, N, d]")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if not (q.shape == k.shape == v.shape):
+        raise ValueError(f"q, k, v shapes differ: {tuple(q.shape)} {tuple(k.shape)} {tuple(v.shape)}")
+    if not (q.device == k.device == v.device):
+        raise ValueError("q, k, v must be on the same device")
+
+
+def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor | None = None,
+           lse: torch.Tensor | None = None, scale: float | None = None, stream=None):
+    """O = softmax(scale * q k^T) v and LSE, by one launch of the fused kernel.
+
+    q, k, v: bf16 CUDA tensors [B, H, N, d], contiguous. ``o`` (bf16 [B,H,N,d])
+    and ``lse`` (float32 [B,H,N]) are allocated with torch when not given.
+    ``scale`` defaults to 1/sqrt(d). Enqueued on ``stream`` (default: torch's
+    current stream for q's device). Returns (o, lse).
+    """
+    _check_qkv(q, k, v)
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if o.dtype != torch.bfloat16 or o.shape != q.shape or not o.is_contiguous() or o.device != q.device:
+        raise ValueError("o must be a contiguous bf16 tensor shaped like q on q's device")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous() \
+            or lse.device != q.device:
+        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor on q's device")
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                        B, H, N, d, float(scale), _stream_handle(stream, q.device))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd")
+    return o, lse
+
+
+def fa_fwd_fault_test(q, k, v, o, lse, scale: float, drop_load: int, timeout_ns: int, stream=None) -> int:
+    """Test hook of the C ABI (see include/fa.h): returns the raw status code."""
+    _check_qkv(q, k, v)
+    B, H, N, d = q.shape
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        return int(lib.fa_fwd_fault_test(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                         B, H, N, d, float(scale), int(drop_load), int(timeout_ns),
+                                         _stream_handle(stream, q.device)))
+
+
+def fa_get_device_status(stream=None, device=None):
+    """Synchronise the stream and read/clear the device status word: (status, info[4])."""
+    lib = load_library()
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    info = (ctypes.c_uint * 4)()
+    with torch.cuda.device(device):
+        st = lib.fa_get_device_status(_stream_handle(stream, device), info)
+    return int(st), [int(x) for x in info]

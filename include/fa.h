@@ -1,0 +1,111 @@
+/*
+ * fa.h -- C ABI of the exact attention forward pass for GB300 (sm_103a).
+ *
+ * The operation: for every batch b and head h,
+ *     S = scale * Q K^T              (N x N scores, never written to memory)
+ *     P = softmax(S) row by row      (safe softmax: subtract the row maximum)
+ *     O = P V                         (N x d, bf16)
+ *     LSE[r] = m_r + ln(sum_j e^{S_rj - m_r})   (one float per query row)
+ * computed in one fused kernel launch that reads Q, K, V once per query
+ * block and writes only O and LSE.
+ *
+ * Sources (page title, then section):
+ *   - "01 · 注意力为什么是 IO 瓶颈" (ai-reference-codex FlashAttention chapter 01),
+ *     §4 (the fused kernel reads Q, K, V and writes only O and LSE) and §6
+ *     (softmax_lse is one float32 per query row; one kernel launch on the
+ *     caller's stream).
+ *   - "Flash Attention (FA1)" (languisher.top), "Naive Attention 问题分析"
+ *     (the safe softmax), "Tiling in FlashAttention" (Br x d query blocks,
+ *     Bc x d key/value blocks, ceil(N/B) blocks) and the derivation of the
+ *     online-softmax update (steps 1-5, boxed O_new equation).
+ *   - "FlashAttention：IO 感知的精确注意力" (inference.xph.ink kp-015), core
+ *     concepts: exact, not approximate; FlashAttention-2 work split.
+ *
+ * Conventions of this library (the pages do not fix an interface):
+ *   - Layout: Q, K, V and O are bf16, contiguous row-major [B, H, N, d]
+ *     (d fastest). LSE is float32, contiguous [B, H, N], natural logarithm of
+ *     the sum of e^{scaled score}: LSE = max_j S_rj + ln(sum_j e^{S_rj - max}).
+ *   - Ownership: the caller allocates every buffer (device memory) and keeps
+ *     ownership; the library allocates no device memory and keeps no pointer
+ *     after the call returns.
+ *   - Asynchrony: fa_fwd only validates its arguments, encodes the TMA
+ *     descriptors and enqueues one kernel on `stream`. Errors found on the
+ *     host are returned immediately and nothing is launched. A device-side
+ *     timeout (a pipeline wait that did not finish within its limit, which a
+ *     correct build never hits) is reported later by fa_get_device_status.
+ *   - Supported: d in {64, 128}; B, H, N >= 1 with B <= 65535, H <= 65535,
+ *     B*H*N < 2^31; scale finite and >= 0; non-causal (no mask).
+ *   - Pointers: Q, K, V, O must be 16-byte aligned, LSE 4-byte aligned. O and
+ *     LSE must not overlap Q, K, V or each other.
+ */
+#ifndef EXACT_IO_AWARE_34_FA_H_
+#define EXACT_IO_AWARE_34_FA_H_
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,  /* null or misaligned pointer, bad size, non-finite scale, overlap */
+  FA_ERR_UNSUPPORTED = 2,  /* a valid request this build does not implement (d, negative scale) */
+  FA_ERR_CUDA = 3,         /* a CUDA runtime or driver call failed; see fa_last_cuda_error() */
+  FA_ERR_TIMEOUT = 4       /* a device-side pipeline wait ran out of time (reported after the fact) */
+} fa_status_t;
+
+/*
+ * fa_fwd -- exact attention forward pass, one kernel launch.
+ *   Q, K, V : device, bf16 [B, H, N, d], read only.
+ *   O       : device, bf16 [B, H, N, d], written (every element).
+ *   LSE     : device, float32 [B, H, N], written (every element).
+ *   B, H, N, d : batch, heads, sequence length, head dimension.
+ *   scale   : multiplies Q K^T before the softmax (1/sqrt(d) is usual).
+ *   stream  : CUDA stream the kernel is enqueued on (0 = legacy default).
+ * Returns FA_OK once the kernel is enqueued; otherwise an error code and
+ * nothing is launched (FA_ERR_CUDA: the launch itself failed).
+ * Follows: "Flash Attention (FA1)" tiling and online-softmax update;
+ * "01 · 注意力为什么是 IO 瓶颈" §4/§6 for the O + LSE outputs.
+ */
+fa_status_t fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                   int B, int H, int N, int d, float scale, cudaStream_t stream);
+
+/*
+ * fa_get_device_status -- synchronise `stream`, then read and clear the
+ * library's device status word on the current device. Returns FA_OK, or
+ * FA_ERR_TIMEOUT if any kernel of this library on this device gave up on a
+ * wait since the last call, or FA_ERR_CUDA if the synchronisation failed.
+ * `info`, if not NULL, receives 4 words describing the first timeout:
+ * {role (1 producer, 2 mma, 3 softmax/epilogue), blockIdx.x, blockIdx.y,
+ * blockIdx.z}; all zero when there was none.
+ */
+fa_status_t fa_get_device_status(cudaStream_t stream, unsigned int* info);
+
+/* fa_status_string -- a static, human-readable name for a status code. */
+const char* fa_status_string(fa_status_t status);
+
+/* fa_last_cuda_error -- the cudaError_t behind the most recent FA_ERR_CUDA
+ * returned on this host thread (0 if none). */
+int fa_last_cuda_error(void);
+
+/*
+ * fa_fwd_fault_test -- TEST HOOK, not for production use. Same as fa_fwd,
+ * but (a) every device-side wait gives up after `timeout_ns` nanoseconds,
+ * and (b) when `drop_load` >= 0 the producer skips the drop_load-th K/V tile
+ * load (0 = K of block 0, 1 = V of block 0, 2 = K of block 1, ...) in every
+ * CTA, so that its consumer's wait runs out. The kernel then stops every role,
+ * waits for its own copies and tensor-core work in flight, frees its tensor
+ * memory and exits normally; fa_get_device_status reports FA_ERR_TIMEOUT and
+ * the CUDA context stays usable. O and LSE are unspecified after a drop.
+ * Exists only to test that the timeout path ends cleanly.
+ */
+fa_status_t fa_fwd_fault_test(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                              int B, int H, int N, int d, float scale,
+                              int drop_load, unsigned long long timeout_ns, cudaStream_t stream);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* EXACT_IO_AWARE_34_FA_H_ */

@@ -1,0 +1,106 @@
+"""Helpers for comparing the CUDA path with the oracle.
+
+Tolerances (bf16 inputs, fp32 accumulation), measured against the float64
+oracle on the identical bf16 inputs:
+  O   max |err|                    <= 2e-2
+  O   ||err||_F / ||O_ref||_F      <= 1e-2
+  LSE max |err|                    <= 1e-3
+  O   max |err| <= 2 x the max |err| of the bf16 materialise-path reference
+      ("01 · 注意力为什么是 IO 瓶颈" §7: no worse than twice the baseline)
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+TOL_O_MAX = 2e-2
+TOL_O_FRO = 1e-2
+TOL_LSE_MAX = 1e-3
+
+
+def to64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def run_gpu(q, k, v, scale, device="cuda:0"):
+    from exact_io_aware_34_gb300 import fa
+    qd, kd, vd = (x.to(device) for x in (q, k, v))
+    o, lse = fa.fa_fwd(qd, kd, vd, scale=scale)
+    torch.cuda.synchronize(device)
+    st, info = fa.fa_get_device_status()
+    assert st == fa.FA_OK, (fa.fa_status_string(st), info)
+    return o.cpu(), lse.cpu()
+
+
+def errors(o_gpu, lse_gpu, O_ref, L_ref):
+    og = to64(o_gpu)
+    lg = to64(lse_gpu)
+    e = og - O_ref
+    return {
+        "o_max": float(np.abs(e).max()) if e.size else 0.0,
+        "o_fro": float(np.linalg.norm(e) / max(np.linalg.norm(O_ref), 1e-300)) if e.size else 0.0,
+        "lse_max": float(np.abs(lg - L_ref).max()) if lg.size else 0.0,
+        "finite": bool(np.isfinite(og).all() and np.isfinite(lg).all()),
+    }
+
+
+def check_full(q, k, v, scale, two_x_rule=True):
+    """Whole-output parity (sizes the oracle evaluates in seconds)."""
+    o, lse = run_gpu(q, k, v, scale)
+    Q, K, V = (to64(x) for x in (q, k, v))
+    O_ref, L_ref = oracle.attention(Q, K, V, scale)
+    err = errors(o, lse, O_ref, L_ref)
+    assert err["finite"], err
+    assert err["o_max"] <= TOL_O_MAX, err
+    assert err["o_fro"] <= TOL_O_FRO, err
+    assert err["lse_max"] <= TOL_LSE_MAX, err
+    if two_x_rule:
+        On = oracle.naive_bf16_attention(Q, K, V, scale)
+        err["naive_o_max"] = float(np.abs(On - O_ref).max())
+        assert err["o_max"] <= 2 * err["naive_o_max"], err
+    return err, o, lse
+
+
+def sample_rows(B, H, N, n, seed=0):
+    """(b, h, r) triples: tile edges, the last rows, and random rows."""
+    rng = np.random.default_rng(seed)
+    picks = set()
+    edges = [0, 1, 127, 128, 255, 256, N - 129, N - 128, N - 1]
+    for b in range(B):
+        for h in (0, H - 1):
+            for r in edges:
+                if 0 <= r < N:
+                    picks.add((b, h, r))
+    while len(picks) < n:
+        picks.add((int(rng.integers(B)), int(rng.integers(H)), int(rng.integers(N))))
+    return np.array(sorted(picks), dtype=np.int64)
+
+
+def check_sampled(q, k, v, scale, n_rows=256, seed=0, two_x_rule=True):
+    """Full-size run on the GPU, compared with the oracle at sampled rows, plus
+    properties every row must have (finite; each O row inside the column-wise
+    range of V, as a convex combination of value rows)."""
+    B, H, N, d = q.shape
+    o, lse = run_gpu(q, k, v, scale)
+    rows = sample_rows(B, H, N, n_rows, seed)
+    O_ref, L_ref = oracle.attention_rows(q.float().numpy(), k.float().numpy(), v.float().numpy(), scale, rows)
+    og = o[rows[:, 0], rows[:, 1], rows[:, 2]]
+    lg = lse[rows[:, 0], rows[:, 1], rows[:, 2]]
+    err = errors(og, lg, O_ref, L_ref)
+    assert err["finite"], err
+    assert err["o_max"] <= TOL_O_MAX, err
+    assert err["o_fro"] <= TOL_O_FRO, err
+    assert err["lse_max"] <= TOL_LSE_MAX, err
+    if two_x_rule:
+        On = oracle.naive_bf16_attention(q.float().numpy(), k.float().numpy(), v.float().numpy(), scale, rows)
+        err["naive_o_max"] = float(np.abs(On - O_ref).max())
+        assert err["o_max"] <= 2 * err["naive_o_max"], err
+    of = o.float()
+    assert torch.isfinite(of).all() and torch.isfinite(lse).all()
+    vmin = v.float().amin(dim=2, keepdim=True)
+    vmax = v.float().amax(dim=2, keepdim=True)
+    slack = 1e-2 * (vmax - vmin) + 1e-6
+    assert bool((of >= vmin - slack).all()) and bool((of <= vmax + slack).all())
+    return err

@@ -1,0 +1,100 @@
+"""The C ABI library: builds, loads, exports every declared symbol, and rejects
+bad arguments on the host before touching the GPU (CPU only)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from exact_io_aware_34_gb300 import build as fa_build
+from exact_io_aware_34_gb300 import fa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa_build.build()
+    return fa.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_\s\*]*?\b(fa_[a-z0-9_]+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    assert names == sorted(fa.EXPORTED), names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", fa.LIB_PATH], capture_output=True, text=True, check=True)
+    exported = set(re.findall(r"\sT\s(\w+)$", out.stdout, re.M))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_status_strings(lib):
+    assert fa.fa_status_string(0) == "FA_OK"
+    assert fa.fa_status_string(1) == "FA_ERR_INVALID_ARG"
+    assert fa.fa_status_string(2) == "FA_ERR_UNSUPPORTED"
+    assert fa.fa_status_string(3) == "FA_ERR_CUDA"
+    assert fa.fa_status_string(4) == "FA_ERR_TIMEOUT"
+    assert fa.fa_status_string(99) == "FA_ERR_UNKNOWN"
+
+
+# Fake, never-dereferenced device addresses: every case below is rejected by
+# the host-side checks before any CUDA call is made.
+A = 0x7F0000000000
+GAP = 1 << 30
+
+
+def call(lib, Q=A, K=A + GAP, V=A + 2 * GAP, O=A + 3 * GAP, L=A + 4 * GAP, B=1, H=1, N=128, d=128, scale=0.1):
+    return lib.fa_fwd(Q, K, V, O, L, B, H, N, d, ctypes.c_float(scale), None)
+
+
+@pytest.mark.parametrize("kwargs,expect", [
+    (dict(Q=0), fa.FA_ERR_INVALID_ARG),
+    (dict(K=0), fa.FA_ERR_INVALID_ARG),
+    (dict(V=0), fa.FA_ERR_INVALID_ARG),
+    (dict(O=0), fa.FA_ERR_INVALID_ARG),
+    (dict(L=0), fa.FA_ERR_INVALID_ARG),
+    (dict(N=0), fa.FA_ERR_INVALID_ARG),
+    (dict(N=-5), fa.FA_ERR_INVALID_ARG),
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(H=0), fa.FA_ERR_INVALID_ARG),
+    (dict(B=70000), fa.FA_ERR_INVALID_ARG),
+    (dict(H=1 << 16), fa.FA_ERR_INVALID_ARG),
+    (dict(B=1024, H=1024, N=4096), fa.FA_ERR_INVALID_ARG),      # B*H*N >= 2^31
+    (dict(d=0), fa.FA_ERR_INVALID_ARG),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=-0.5), fa.FA_ERR_UNSUPPORTED),
+    (dict(Q=A + 8), fa.FA_ERR_INVALID_ARG),                     # not 16-byte aligned
+    (dict(O=A + 3 * GAP + 4), fa.FA_ERR_INVALID_ARG),
+    (dict(L=A + 4 * GAP + 2), fa.FA_ERR_INVALID_ARG),
+    (dict(O=A + 1024), fa.FA_ERR_INVALID_ARG),                  # O overlaps Q
+    (dict(L=A + 2 * GAP + 64), fa.FA_ERR_INVALID_ARG),          # LSE overlaps V
+    (dict(L=A + 3 * GAP + 128), fa.FA_ERR_INVALID_ARG),         # LSE overlaps O
+])
+def test_host_side_rejections(lib, kwargs, expect):
+    assert call(lib, **kwargs) == expect
+
+
+def test_fault_hook_rejects_zero_timeout(lib):
+    st = lib.fa_fwd_fault_test(A, A + GAP, A + 2 * GAP, A + 3 * GAP, A + 4 * GAP, 1, 1, 128, 128,
+                               ctypes.c_float(0.1), 0, 0, None)
+    assert st == fa.FA_ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    monkeypatch.setattr(fa, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        fa.load_library(str(tmp_path / "libfa.so"))

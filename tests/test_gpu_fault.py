@@ -1,0 +1,50 @@
+"""Device-side wait limits: a K/V tile that never arrives ends the kernel with a
+timeout status instead of a hang, and the context stays usable (needs a GB300).
+
+The failure is made without faulting the GPU: the test hook tells the
+producer to skip one TMA load, so its consumer's wait runs out after a short
+limit. Every role then stops, waits for its own copies and MMAs in flight,
+frees tensor memory and returns.
+"""
+import math
+
+import pytest
+import torch
+
+import oracle
+from exact_io_aware_34_gb300 import fa, inputs
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("drop", [0, 1, 2, 5])
+def test_dropped_load_times_out_cleanly(d, drop):
+    B, H, N = 1, 2, 700
+    q, k, v = inputs.make_random(B, H, N, d, seed=20 + drop)
+    qd, kd, vd = (x.cuda() for x in (q, k, v))
+    o = torch.zeros_like(qd)
+    lse = torch.zeros(B, H, N, dtype=torch.float32, device="cuda")
+    st = fa.fa_fwd_fault_test(qd, kd, vd, o, lse, 1 / math.sqrt(d), drop, 20_000_000)   # 20 ms
+    assert st == fa.FA_OK
+    st, info = fa.fa_get_device_status()
+    assert st == fa.FA_ERR_TIMEOUT, (st, info)
+    assert info[0] in (1, 2, 3)
+    assert fa.fa_get_device_status()[0] == fa.FA_OK          # the status word was cleared
+    # the context is still usable and the next call is correct
+    s = 1 / math.sqrt(d)
+    o2, lse2 = fa.fa_fwd(qd, kd, vd, scale=s)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status()[0] == fa.FA_OK
+    O_ref, L_ref = oracle.attention(*(parity.to64(x) for x in (q, k, v)), s)
+    err = parity.errors(o2.cpu(), lse2.cpu(), O_ref, L_ref)
+    assert err["o_max"] <= parity.TOL_O_MAX and err["lse_max"] <= parity.TOL_LSE_MAX, err
+
+
+def test_drop_beyond_last_load_is_harmless():
+    q, k, v = (x.cuda() for x in inputs.make_random(1, 1, 256, 128, seed=30))
+    o = torch.empty_like(q)
+    lse = torch.empty(1, 1, 256, dtype=torch.float32, device="cuda")
+    assert fa.fa_fwd_fault_test(q, k, v, o, lse, 0.1, 10_000, 20_000_000) == fa.FA_OK
+    assert fa.fa_get_device_status()[0] == fa.FA_OK
