@@ -1,0 +1,76 @@
+"""Host-side logic of bench.py (CPU only): the max-over-ranks reduction with two
+gloo ranks, clock parsing, peaks and the traffic record's source-hash check."""
+import json
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank_main(rank, world, port, out):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    w, r, local = bench.dist_setup()
+    assert (w, r, local) == (world, rank, rank)
+    bench.barrier(w)
+    # per-rank summed step time: the job's time is the slowest rank's
+    m = bench.reduce_max(10.0 + 5.0 * rank, w)
+    out[rank] = m
+    bench.barrier(w)
+    dist.destroy_process_group()
+
+
+def test_reduce_max_two_gloo_ranks():
+    world = 2
+    port = _free_port()
+    with mp.Manager() as man:
+        out = man.dict()
+        mp.spawn(_rank_main, args=(world, port, out), nprocs=world, join=True)
+        assert dict(out) == {0: 15.0, 1: 15.0}
+
+
+def test_reduce_max_single_rank_is_identity():
+    assert bench.reduce_max(3.25, 1) == 3.25
+
+
+def test_clock_summary_parsing():
+    c = bench.ClockSampler(0)
+    c.out = "\n".join([
+        "0, 1900, 2070, 900.5, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "0, 1950, 2070, 1100.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "0, 2000, 2070, 1200.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+    ])
+    s = c.summary()
+    assert s["sm_mhz"] == 1950 and s["sm_max_mhz"] == 2070
+    assert s["reasons"] == ["sw_power_cap"] and s["samples"] == 3
+
+
+def test_peaks_and_traffic(tmp_path, monkeypatch):
+    peaks, src = bench.load_peaks()
+    assert peaks["bf16_tflops"] > 100 and src in ("measured", "fallback")
+    rec = {"prefill8k_d128_h32": {"kernel_source_hash": bench.kernel_source_hash(), "dram_bytes_per_launch": 123}}
+    p = tmp_path / "t.json"
+    p.write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(p))
+    assert bench.load_traffic("prefill8k_d128_h32") == 123
+    rec["prefill8k_d128_h32"]["kernel_source_hash"] = "stale"
+    p.write_text(json.dumps(rec))
+    assert bench.load_traffic("prefill8k_d128_h32") is None
+
+
+def test_warmup_floor():
+    with pytest.raises(SystemExit):
+        bench.main(["--warmup", "2"])
