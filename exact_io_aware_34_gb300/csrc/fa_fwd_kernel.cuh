@@ -352,18 +352,26 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
       for (int c = 0; c < 4; ++c) ptx::reg_fence32(s[c]);
 
       const int valid = p.N - j * C::kBN;    // keys of this block that exist
-      if (valid < C::kBN) {
+      const bool ragged = valid < C::kBN;
+      if (ragged) {
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int i = 0; i < 32; ++i)
             if (32 * c + i >= valid) s[c][i] = __float_as_uint(-INFINITY);
       }
-      float mt = -INFINITY;
+      // Row maximum: 8 independent chains of 3-input max, then a small tree.
+      float mc[8];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int k = 0; k < 8; ++k) {
+        const int c = k >> 1, b = (k & 1) * 16;
+        mc[k] = fmaxf(__uint_as_float(s[c][b]), __uint_as_float(s[c][b + 1]));
 #pragma unroll
-        for (int i = 0; i < 32; ++i) mt = fmaxf(mt, __uint_as_float(s[c][i]));
+        for (int i = 2; i < 16; i += 2)
+          mc[k] = ptx::max3(mc[k], __uint_as_float(s[c][b + i]), __uint_as_float(s[c][b + i + 1]));
+      }
+      const float mt = ptx::max3(ptx::max3(mc[0], mc[1], mc[2]), ptx::max3(mc[3], mc[4], mc[5]),
+                                 fmaxf(mc[6], mc[7]));
 
       float alpha = 1.f;
       bool rescale_o = false;
@@ -377,22 +385,37 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
           m_use = mt;
         }
       }
+      // P = 2^(s*scale*log2e - m*scale*log2e): pairs through the f32x2 FMA,
+      // MUFU ex2 per element, 4 independent f32x2 partial sums, bf16x2 pack.
+      const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
       const float neg_m = -m_use * sl2;
-      float sum = 0.f;
+      const uint64_t negmx2 = ptx::f2_pack(neg_m, neg_m);
+      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
       uint32_t pk[2][32];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          float p0 = ptx::ex2_approx(fmaf(__uint_as_float(s[c][i]), sl2, neg_m));
-          float p1 = ptx::ex2_approx(fmaf(__uint_as_float(s[c][i + 1]), sl2, neg_m));
-          if (valid < C::kBN) {
+          float x0, x1;
+          ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[c][i]), __uint_as_float(s[c][i + 1])), sl2x2,
+                                     negmx2),
+                         x0, x1);
+          float p0 = ptx::ex2_approx(x0);
+          float p1 = ptx::ex2_approx(x1);
+          if (ragged) {   // exact zeros for keys past N (also when scale == 0)
             if (32 * c + i >= valid) p0 = 0.f;
             if (32 * c + i + 1 >= valid) p1 = 0.f;
           }
-          sum += p0 + p1;
+          acc[(i >> 1) & 3] = ptx::f2_add(acc[(i >> 1) & 3], ptx::f2_pack(p0, p1));
           pk[c >> 1][(c & 1) * 16 + (i >> 1)] = ptx::pack_bf16x2(p0, p1);
         }
+      }
+      float sum;
+      {
+        float a0, a1, b0, b1;
+        ptx::f2_unpack(ptx::f2_add(acc[0], acc[1]), a0, a1);
+        ptx::f2_unpack(ptx::f2_add(acc[2], acc[3]), b0, b1);
+        sum = (a0 + a1) + (b0 + b1);
       }
       l = l * alpha + sum;
       ptx::tmem_st32(tS, pk[0]);
