@@ -77,27 +77,78 @@ def load_traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
-    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
-              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
-              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+    """SM clock, power and clock-event (throttle) reasons sampled every few ms
+    while the timed region runs: NVML through ctypes in a background thread,
+    or ``nvidia-smi -lms 200`` when NVML cannot be loaded."""
+    # nvmlClocksEventReasons bits (nvml.h)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+    SMI_FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+                  "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+                  "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, uuid: str | None = None, period_s: float = 0.005):
         self.gpu = gpu_index
+        self.uuid = uuid
+        self.period = period_s
+        self.samples = []          # (sm_mhz, power_w, reason_bits)
+        self.max_mhz = None
+        self.out = ""
         self.proc = None
+        self._thread = None
+        self._stop = False
+        self._nvml = None
+
+    def _nvml_open(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        ok = False
+        if self.uuid:
+            ok = lib.nvmlDeviceGetHandleByUUID(("GPU-" + self.uuid).encode(), ctypes.byref(h)) == 0
+        if not ok and lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.gpu), ctypes.byref(h)) != 0:
+            raise OSError("no NVML handle")
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+            self.max_mhz = float(mx.value)
+        reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        return lib, h, reasons_fn
+
+    def _nvml_loop(self):
+        import ctypes
+        lib, h, reasons_fn = self._nvml
+        clk, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop:
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                p = pw.value / 1000.0 if lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw)) == 0 else None
+                r = rs.value if reasons_fn(h, ctypes.byref(rs)) == 0 else 0
+                self.samples.append((float(clk.value), p, int(r)))
+            time.sleep(self.period)
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", "--query-gpu=" + ",".join(self.FIELDS),
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
+            self._nvml = self._nvml_open()
+            import threading
+            self._thread = threading.Thread(target=self._nvml_loop, daemon=True)
+            self._thread.start()
+        except (OSError, AttributeError):
+            self._nvml = None
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", f"--id={self.gpu}", "--query-gpu=" + ",".join(self.SMI_FIELDS),
+                     "--format=csv,noheader,nounits", "-lms", "200"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except OSError:
+                self.proc = None
         return self
 
     def __exit__(self, *exc):
-        self.out = ""
+        if self._thread is not None:
+            self._stop = True
+            self._thread.join(timeout=2)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -108,8 +159,15 @@ class ClockSampler:
         return False
 
     def summary(self):
+        if self.samples:
+            sm = [c for c, _, _ in self.samples]
+            power = [p for _, p, _ in self.samples if p is not None]
+            reasons = sorted({name for _, _, r in self.samples for bit, name in self.REASONS.items() if r & bit})
+            return {"sm_mhz": statistics.median(sm), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                    "samples": len(sm), "sm_mhz_min": min(sm), "power_w_max": max(power) if power else None,
+                    "source": "nvml"}
         rows = [r.split(", ") for r in (self.out or "").strip().splitlines() if r.strip()]
-        rows = [r for r in rows if len(r) == len(self.FIELDS)]
+        rows = [r for r in rows if len(r) == len(self.SMI_FIELDS)]
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
         sm = [float(r[1]) for r in rows if r[1].replace(".", "", 1).isdigit()]
@@ -118,7 +176,8 @@ class ClockSampler:
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
         power = [float(r[3]) for r in rows if r[3].replace(".", "", 1).isdigit()]
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None,
+                "source": "nvidia-smi"}
 
 
 def dist_setup():
@@ -321,8 +380,12 @@ def run_native(args):
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier(world, device)
     torch.cuda.synchronize(device)
-    with ClockSampler(local) as clocks:
-        time.sleep(0.3)
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        pass
+    with ClockSampler(local, uuid) as clocks:
         for i in range(args.steps):
             flush.fill_(float(i))
             starts[i].record(stream)
@@ -397,7 +460,7 @@ def run_native(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)

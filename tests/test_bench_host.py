@@ -74,3 +74,12 @@ def test_peaks_and_traffic(tmp_path, monkeypatch):
 def test_warmup_floor():
     with pytest.raises(SystemExit):
         bench.main(["--warmup", "2"])
+
+
+def test_clock_summary_nvml_samples():
+    c = bench.ClockSampler(0)
+    c.samples = [(1900.0, 900.0, 0x4), (1950.0, 1000.0, 0), (2000.0, 1100.0, 0x8)]
+    c.max_mhz = 2070.0
+    s = c.summary()
+    assert s["sm_mhz"] == 1950.0 and s["sm_max_mhz"] == 2070.0 and s["source"] == "nvml"
+    assert s["reasons"] == ["hw_slowdown", "sw_power_cap"] and s["samples"] == 3
