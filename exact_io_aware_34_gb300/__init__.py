@@ -15,6 +15,8 @@ from .fa import (  # noqa: F401
     fa_fwd_fault_test,
     fa_get_device_status,
     fa_last_cuda_error,
+    fa_naive_fwd,
+    fa_naive_workspace_bytes,
     fa_status_string,
     load_library,
 )

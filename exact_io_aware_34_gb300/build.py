@@ -15,7 +15,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libfa.so")
 SOURCES = [os.path.join(CSRC, "fa_api.cu")]
-DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("fa_fwd_kernel.cuh", "sm103a_ptx.cuh")] + [
+DEPENDS = SOURCES + sorted(
+    os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".cu"))) + [
     os.path.join(os.path.dirname(PKG), "include", "fa.h")]
 
 NVCC_FLAGS = [

@@ -16,10 +16,14 @@
 
 #include "../../include/fa.h"
 #include "fa_fwd_kernel.cuh"
+#include "naive_kernels.cuh"
 
 namespace {
 
 thread_local int t_last_cuda_error = 0;
+
+// Bound on every device-side wait of the standard-attention kernels.
+constexpr unsigned long long kNaiveTimeoutNs = 2000000000ull;
 
 fa_status_t cuda_fail(cudaError_t e) {
   t_last_cuda_error = static_cast<int>(e);
@@ -122,6 +126,100 @@ fa_status_t fwd_impl(const void* Q, const void* K, const void* V, void* O, float
   return launch<128>(Q, K, V, O, LSE, B, H, N, scale, drop_load, timeout_ns, stream);
 }
 
+// ---------------------------------------------------------------- standard attention
+// Row stride (elements) of the N x N score / probability matrices in the
+// workspace: a multiple of 64 so that every row starts 128-byte aligned.
+inline long long naive_ld(int N) { return (static_cast<long long>(N) + 63) / 64 * 64; }
+
+// 3-D bf16 map [Z][rows][cols] with a row stride of ld elements.
+bool make_map_ld(CUtensorMap* m, const void* base, int Z, int rows, int cols, long long ld, int box_cols,
+                 int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(Z)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2, static_cast<cuuint64_t>(ld) * rows * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, bool B_KMAJOR>
+cudaError_t gemm_attr() {
+  using G = fa::naive::GemmCfg<BN, B_KMAJOR>;
+  return cudaFuncSetAttribute(fa::naive::gemm_bf16_kernel<BN, B_KMAJOR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              G::kSmemBytes);
+}
+
+// The three launches of standard attention with S / P in `ws` ([B*H][N][ld] bf16).
+template <int HD>
+fa_status_t naive_launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N,
+                         float scale, void* ws, cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= 64) return FA_ERR_UNSUPPORTED;
+  static std::once_flag once[64];
+  static cudaError_t attr_err[64];
+  std::call_once(once[dev], [&] {
+    attr_err[dev] = gemm_attr<128, true>();
+    if (attr_err[dev] == cudaSuccess) attr_err[dev] = gemm_attr<HD, false>();
+  });
+  if (attr_err[dev] != cudaSuccess) return cuda_fail(attr_err[dev]);
+
+  const int BH = B * H;
+  const long long ld = naive_ld(N);
+  CUtensorMap mq, mk, mp, mv;
+  if (!make_map_ld(&mq, Q, BH, N, HD, HD, 64, 128) || !make_map_ld(&mk, K, BH, N, HD, HD, 64, 128) ||
+      !make_map_ld(&mp, ws, BH, N, N, ld, 64, 128) || !make_map_ld(&mv, V, BH, N, HD, HD, 64, 64))
+    return cuda_fail(cudaErrorInvalidValue);
+  auto* S = static_cast<__nv_bfloat16*>(ws);
+
+  // 1. S = bf16(scale * bf16(Q K^T))
+  fa::naive::GemmParams g1{S, N, N, HD, static_cast<int>(ld), scale, kNaiveTimeoutNs};
+  using G1 = fa::naive::GemmCfg<128, true>;
+  fa::naive::gemm_bf16_kernel<128, true><<<dim3((N + 127) / 128, (N + 127) / 128, BH), G1::kThreads, G1::kSmemBytes,
+                                           stream>>>(mq, mk, g1);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  // 2. P = softmax(S) row by row, in place; LSE = m + ln l
+  fa::naive::softmax_rows_kernel<<<static_cast<unsigned>(static_cast<long long>(BH) * N), 256, 0, stream>>>(
+      S, LSE, N, static_cast<int>(ld));
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  // 3. O = bf16(P V)
+  fa::naive::GemmParams g2{static_cast<__nv_bfloat16*>(O), N, HD, N, HD, 1.0f, kNaiveTimeoutNs};
+  using G2 = fa::naive::GemmCfg<HD, false>;
+  fa::naive::gemm_bf16_kernel<HD, false><<<dim3(1, (N + 127) / 128, BH), G2::kThreads, G2::kSmemBytes, stream>>>(
+      mp, mv, g2);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FA_OK;
+}
+
+// Argument checks shared by every entry point of the library (host side only).
+fa_status_t check_args(const void* Q, const void* K, const void* V, const void* O, const float* LSE, int B, int H,
+                       int N, int d, float scale) {
+  if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+  if (B > 65535 || H > 65535) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H * N >= (1LL << 31)) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (scale < 0.f) return FA_ERR_UNSUPPORTED;
+  for (const void* ptr : {Q, K, V, O})
+    if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return FA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(LSE) % 4 != 0) return FA_ERR_INVALID_ARG;
+  const size_t n_qkv = static_cast<size_t>(B) * H * N * d * 2;
+  const size_t n_lse = static_cast<size_t>(B) * H * N * 4;
+  for (const void* in : {Q, K, V}) {
+    if (overlaps(O, n_qkv, in, n_qkv) || overlaps(LSE, n_lse, in, n_qkv)) return FA_ERR_INVALID_ARG;
+  }
+  if (overlaps(O, n_qkv, LSE, n_lse)) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
 // A correct pipeline never waits anywhere near this long; it only bounds
 // how long a broken one can hold the GPU.
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
@@ -161,6 +259,27 @@ fa_status_t fa_get_device_status(cudaStream_t stream, unsigned int* info) {
   if (e == cudaSuccess) e = cudaMemcpyToSymbol(fa::g_status_info, zeros, sizeof(zeros));
   if (e != cudaSuccess) return cuda_fail(e);
   return FA_ERR_TIMEOUT;
+}
+
+size_t fa_naive_workspace_bytes(int B, int H, int N) {
+  if (B < 1 || H < 1 || N < 1) return 0;
+  return static_cast<size_t>(B) * H * N * naive_ld(N) * 2;
+}
+
+fa_status_t fa_naive_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N,
+                         int d, float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  fa_status_t st = check_args(Q, K, V, O, LSE, B, H, N, d, scale);
+  if (st != FA_OK) return st;
+  if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 128 != 0) return FA_ERR_INVALID_ARG;
+  const size_t need = fa_naive_workspace_bytes(B, H, N);
+  if (workspace_bytes < need) return FA_ERR_INVALID_ARG;
+  const size_t n_qkv = static_cast<size_t>(B) * H * N * d * 2;
+  const size_t n_lse = static_cast<size_t>(B) * H * N * 4;
+  for (const void* in : {Q, K, V, static_cast<const void*>(O)})
+    if (overlaps(workspace, need, in, n_qkv)) return FA_ERR_INVALID_ARG;
+  if (overlaps(workspace, need, LSE, n_lse)) return FA_ERR_INVALID_ARG;
+  if (d == 64) return naive_launch<64>(Q, K, V, O, LSE, B, H, N, scale, workspace, stream);
+  return naive_launch<128>(Q, K, V, O, LSE, B, H, N, scale, workspace, stream);
 }
 
 const char* fa_status_string(fa_status_t status) {

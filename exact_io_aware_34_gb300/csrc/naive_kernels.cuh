@@ -1,0 +1,267 @@
+// Standard (materialising) attention on GB300: the comparator for the fused
+// kernel. It runs the three steps that "01 · 注意力为什么是 IO 瓶颈" §3 and §5
+// describe, each as its own kernel with its N x N intermediate in HBM:
+//   1. S = bf16(scale * bf16(Q K^T))      gemm_bf16_kernel (tcgen05, TMEM)
+//   2. P = bf16(softmax(S)) in place of S; LSE = m + ln l per row
+//                                          softmax_rows_kernel
+//   3. O = bf16(P V)                        gemm_bf16_kernel
+// The rounding points are those of a bf16 framework running the three ops
+// (the reading used for the "no worse than twice the baseline" rule).
+//
+// gemm_bf16_kernel computes, for every batch index z (one (b, h)):
+//   C[z][m][n] = bf16(alpha * bf16(sum_k A[z][m][k] * B[z](k, n)))
+// with A row-major [M][K] (K-major operand) and B either [Nc][K] (K-major,
+// for S = Q K^T) or [K][Nc] (MN-major, for O = P V). One CTA computes a
+// 128 x BN tile of C; warp 4 loads A and B chunks of 64 k with TMA into a
+// ring, warp 5 issues the tcgen05 MMAs into TMEM, warps 0-3 convert and
+// store the accumulator (one row per thread).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "sm103a_ptx.cuh"
+
+namespace fa {
+namespace naive {
+
+template <int BN, bool B_KMAJOR>
+struct GemmCfg {
+  static constexpr int kBM = 128;
+  static constexpr int kBK = 64;                          // k per ring stage (one 128-byte row)
+  static constexpr int kABytes = kBM * kBK * 2;           // 16 KB
+  static constexpr int kBBytes = BN * kBK * 2;            // BN x 64 bf16
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = 4;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
+  static constexpr int kThreads = 192;                    // 6 warps
+  static constexpr uint32_t kTmemCols = BN < 32 ? 32 : BN;
+  static constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kBM, BN, false, !B_KMAJOR);
+};
+
+struct GemmParams {
+  __nv_bfloat16* C;
+  int M, Nc, K;
+  int ldc;          // row stride of C in elements (a multiple of 8)
+  float alpha;
+  unsigned long long timeout_ns;
+};
+
+// Bounded single-thread wait; on timeout records the status word and
+// returns false (the caller then stops issuing and drains).
+__device__ __forceinline__ bool naive_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                           unsigned long long timeout_ns, unsigned int role) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (ptx::globaltimer_ns() - t0 > timeout_ns) {
+      *abort_flag = 1;
+      if (atomicCAS(&g_status_word, 0u, 1u) == 0u) {
+        g_status_info[0] = role;
+        g_status_info[1] = blockIdx.x;
+        g_status_info[2] = blockIdx.y;
+        g_status_info[3] = blockIdx.z;
+      }
+      __threadfence();
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ bool naive_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                unsigned long long timeout_ns, unsigned int role) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = naive_wait(bar, parity, abort_flag, timeout_ns, role) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+template <int BN, bool B_KMAJOR>
+__global__ void __launch_bounds__(GemmCfg<BN, B_KMAJOR>::kThreads, 1)
+    gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const GemmParams p) {
+  using C = GemmCfg<BN, B_KMAJOR>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_full[C::kStages];
+  __shared__ __align__(8) uint64_t bar_empty[C::kStages];
+  __shared__ __align__(8) uint64_t bar_acc;
+  __shared__ __align__(8) uint64_t bar_drain;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * BN;
+  const int m0 = blockIdx.y * C::kBM;
+  const int z = blockIdx.z;
+  const int nk = (p.K + C::kBK - 1) / C::kBK;
+  const uint32_t base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&bar_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bar_empty[s]), 1);
+    }
+    ptx::mbar_init(ptx::smem_u32(&bar_acc), 1);
+    ptx::mbar_init(ptx::smem_u32(&bar_drain), 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 5) {
+    ptx::tmem_alloc(ptx::smem_u32(&tmem_slot), C::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  volatile int* abort_ptr = &abort_flag;
+
+  if (warp == 4) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol = ptx::policy_evict_first();
+      int issued = 0;
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % C::kStages;
+        if (!naive_wait(ptx::smem_u32(&bar_empty[s]), ((kb / C::kStages) & 1) ^ 1u, abort_ptr, p.timeout_ns, 1))
+          break;
+        issued = kb + 1;
+        const uint32_t full = ptx::smem_u32(&bar_full[s]);
+        const uint32_t sa = base + s * C::kStageBytes;
+        const uint32_t sb = sa + C::kABytes;
+        ptx::mbar_arrive_expect_tx(full, C::kStageBytes);
+        ptx::tma_load_3d(sa, &tmA, full, kb * C::kBK, m0, z, pol);
+        if (B_KMAJOR) {
+          ptx::tma_load_3d(sb, &tmB, full, kb * C::kBK, n0, z, pol);
+        } else {
+          // BN columns of n as BN/64 boxes of 64 n x 64 k rows (8 KB each).
+#pragma unroll
+          for (int c = 0; c < BN / 64; ++c) ptx::tma_load_3d(sb + c * 8192, &tmB, full, n0 + 64 * c, kb * C::kBK, z, pol);
+        }
+      }
+      if (*abort_ptr) {
+        const int first = issued > C::kStages ? issued - C::kStages : 0;
+        for (int kb = first; kb < issued; ++kb) drain_wait(ptx::smem_u32(&bar_full[kb % C::kStages]), (kb / C::kStages) & 1, p.timeout_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = true;
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % C::kStages;
+        ok = naive_wait(ptx::smem_u32(&bar_full[s]), (kb / C::kStages) & 1, abort_ptr, p.timeout_ns, 2);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const uint32_t sa = base + s * C::kStageBytes;
+        const uint32_t sb = sa + C::kABytes;
+#pragma unroll
+        for (int kk = 0; kk < C::kBK / 16; ++kk) {
+          const uint64_t adesc = ptx::desc_kmajor_sw128(sa + kk * 32);
+          const uint64_t bdesc = B_KMAJOR ? ptx::desc_kmajor_sw128(sb + kk * 32)
+                                          : ptx::desc_mnmajor_sw128(sb + kk * 16 * 128, 8192);
+          ptx::mma_ss(tmem, adesc, bdesc, C::kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
+        }
+        ptx::mma_commit(ptx::smem_u32(&bar_empty[s]));
+      }
+      if (ok) {
+        ptx::mma_commit(ptx::smem_u32(&bar_acc));
+      } else {
+        ptx::mma_commit(ptx::smem_u32(&bar_drain));
+        drain_wait(ptx::smem_u32(&bar_drain), 0, p.timeout_ns);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ epilogue: one row per thread
+    if (naive_wait_warp(ptx::smem_u32(&bar_acc), 0, abort_ptr, p.timeout_ns, 3)) {
+      ptx::tc_fence_after();
+      const int row = warp * 32 + lane;
+      const int m = m0 + row;
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+      __nv_bfloat16* crow = p.C + (static_cast<size_t>(z) * p.M + m) * p.ldc + n0;
+      const bool full_row = n0 + BN <= p.Nc;
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t acc[32];
+        ptx::tmem_ld32(taddr + 32 * c, acc);
+        ptx::tmem_ld_wait();
+        ptx::reg_fence32(acc);
+        if (m < p.M) {
+          uint32_t packed[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            // round the fp32 sum to bf16, then apply alpha and round again
+            const float a0 = __bfloat162float(__float2bfloat16_rn(__uint_as_float(acc[2 * i]))) * p.alpha;
+            const float a1 = __bfloat162float(__float2bfloat16_rn(__uint_as_float(acc[2 * i + 1]))) * p.alpha;
+            packed[i] = ptx::pack_bf16x2(a0, a1);
+          }
+          if (full_row) {
+            uint4* dst = reinterpret_cast<uint4*>(crow + 32 * c);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+          } else {
+            const __nv_bfloat16* vals = reinterpret_cast<const __nv_bfloat16*>(packed);
+            for (int i = 0; i < 32; ++i)
+              if (n0 + 32 * c + i < p.Nc) crow[32 * c + i] = vals[i];
+          }
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// Row softmax in place: P[r] = bf16(e^{S[r] - m} / l) computed in fp32 from
+// the bf16 scores, LSE[r] = m + ln l. One CTA of 256 threads per row; rows
+// have n valid columns and a stride of ld elements.
+__global__ void __launch_bounds__(256) softmax_rows_kernel(__nv_bfloat16* S, float* LSE, int n, int ld) {
+  const size_t r = blockIdx.x;
+  __nv_bfloat16* row = S + r * static_cast<size_t>(ld);
+  __shared__ float red_m[8], red_l[8];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // pass 1: online max and sum of exponentials
+  float m = -INFINITY, l = 0.f;
+  for (int i = tid; i < n; i += 256) {
+    const float x = __bfloat162float(row[i]);
+    if (x > m) {
+      l = l * expf(m - x) + 1.f;
+      m = x;
+    } else {
+      l += expf(x - m);
+    }
+  }
+  for (int off = 16; off > 0; off >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+    const float l2 = __shfl_xor_sync(0xffffffffu, l, off);
+    const float mn = fmaxf(m, m2);
+    l = (m == -INFINITY ? 0.f : l * expf(m - mn)) + (m2 == -INFINITY ? 0.f : l2 * expf(m2 - mn));
+    m = mn;
+  }
+  if (lane == 0) {
+    red_m[warp] = m;
+    red_l[warp] = l;
+  }
+  __syncthreads();
+  float mt = red_m[0];
+  for (int w = 1; w < 8; ++w) mt = fmaxf(mt, red_m[w]);
+  float lt = 0.f;
+  for (int w = 0; w < 8; ++w) lt += red_m[w] == -INFINITY ? 0.f : red_l[w] * expf(red_m[w] - mt);
+  // pass 2: write P over S
+  const float inv = 1.f / lt;
+  for (int i = tid; i < n; i += 256) row[i] = __float2bfloat16_rn(expf(__bfloat162float(row[i]) - mt) * inv);
+  if (tid == 0) LSE[r] = mt + logf(lt);
+}
+
+}  // namespace naive
+}  // namespace fa

@@ -24,7 +24,8 @@ FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
 
 #: every symbol include/fa.h declares
-EXPORTED = ("fa_fwd", "fa_get_device_status", "fa_status_string", "fa_last_cuda_error", "fa_fwd_fault_test")
+EXPORTED = ("fa_fwd", "fa_get_device_status", "fa_status_string", "fa_last_cuda_error", "fa_fwd_fault_test",
+            "fa_naive_fwd", "fa_naive_workspace_bytes")
 
 _lib = None
 
@@ -57,6 +58,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_last_cuda_error.argtypes = []
     lib.fa_last_cuda_error.restype = i
+    lib.fa_naive_workspace_bytes.argtypes = [i, i, i]
+    lib.fa_naive_workspace_bytes.restype = ctypes.c_size_t
+    lib.fa_naive_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, vp, ctypes.c_size_t, vp]
+    lib.fa_naive_fwd.restype = i
     _lib = lib
     return lib
 
@@ -121,6 +126,36 @@ def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor | 
                         B, H, N, d, float(scale), _stream_handle(stream, q.device))
     if st != FA_OK:
         raise FaError(st, "fa_fwd")
+    return o, lse
+
+
+def fa_naive_workspace_bytes(B: int, H: int, N: int) -> int:
+    return int(load_library().fa_naive_workspace_bytes(int(B), int(H), int(N)))
+
+
+def fa_naive_fwd(q, k, v, o=None, lse=None, scale: float | None = None, workspace=None, stream=None):
+    """Standard attention with S and P materialised in ``workspace`` (the
+    comparator of the fused kernel). ``workspace`` is a CUDA tensor of at least
+    fa_naive_workspace_bytes(B, H, N) bytes; allocated with torch when None.
+    Returns (o, lse)."""
+    _check_qkv(q, k, v)
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    need = fa_naive_workspace_bytes(B, H, N)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.fa_naive_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
+                              float(scale), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                              _stream_handle(stream, q.device))
+    if st != FA_OK:
+        raise FaError(st, "fa_naive_fwd")
     return o, lse
 
 

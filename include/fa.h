@@ -41,6 +41,7 @@
 #ifndef EXACT_IO_AWARE_34_FA_H_
 #define EXACT_IO_AWARE_34_FA_H_
 
+#include <stddef.h>
 #include <cuda_runtime_api.h>
 
 #ifdef __cplusplus
@@ -88,6 +89,30 @@ const char* fa_status_string(fa_status_t status);
 /* fa_last_cuda_error -- the cudaError_t behind the most recent FA_ERR_CUDA
  * returned on this host thread (0 if none). */
 int fa_last_cuda_error(void);
+
+/*
+ * fa_naive_workspace_bytes -- bytes of device workspace fa_naive_fwd needs for
+ * B x H heads of length N: the N x N score matrix of every head in bf16,
+ * rows padded to a multiple of 64 elements. Returns 0 for non-positive sizes.
+ */
+size_t fa_naive_workspace_bytes(int B, int H, int N);
+
+/*
+ * fa_naive_fwd -- standard attention with the N x N intermediates in HBM:
+ * the comparator the fused kernel is measured against. Three kernel launches
+ * on `stream`, as "01 · 注意力为什么是 IO 瓶颈" §3 and §5 describe:
+ *   S = bf16(scale * bf16(Q K^T))   (written to `workspace`)
+ *   P = bf16(softmax(S))            (written over S; LSE = m + ln l per row)
+ *   O = bf16(P V)
+ * Arguments as for fa_fwd, plus `workspace`: device memory of at least
+ * fa_naive_workspace_bytes(B, H, N) bytes, 128-byte aligned, owned by the
+ * caller, not overlapping any other buffer; its contents are overwritten.
+ * Same shape limits and error codes as fa_fwd; FA_ERR_INVALID_ARG also for
+ * a missing, misaligned, too small or overlapping workspace.
+ */
+fa_status_t fa_naive_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                         int B, int H, int N, int d, float scale,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * fa_fwd_fault_test -- TEST HOOK, not for production use. Same as fa_fwd,

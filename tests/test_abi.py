@@ -98,3 +98,29 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(fa, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         fa.load_library(str(tmp_path / "libfa.so"))
+
+
+def naive_call(lib, ws=A + 6 * GAP, ws_bytes=1 << 40, **kw):
+    args = dict(Q=A, K=A + GAP, V=A + 2 * GAP, O=A + 3 * GAP, L=A + 4 * GAP, B=1, H=1, N=128, d=128, scale=0.1)
+    args.update(kw)
+    return lib.fa_naive_fwd(args["Q"], args["K"], args["V"], args["O"], args["L"], args["B"], args["H"], args["N"],
+                            args["d"], ctypes.c_float(args["scale"]), ws, ws_bytes, None)
+
+
+def test_naive_workspace_size(lib):
+    assert fa.fa_naive_workspace_bytes(1, 1, 128) == 128 * 128 * 2
+    assert fa.fa_naive_workspace_bytes(2, 3, 100) == 6 * 100 * 128 * 2      # rows padded to 64 elements
+    assert fa.fa_naive_workspace_bytes(0, 1, 128) == 0
+
+
+@pytest.mark.parametrize("kwargs,expect", [
+    (dict(ws=0), fa.FA_ERR_INVALID_ARG),
+    (dict(ws=A + 6 * GAP + 64), fa.FA_ERR_INVALID_ARG),        # not 128-byte aligned
+    (dict(ws_bytes=128 * 128 * 2 - 1), fa.FA_ERR_INVALID_ARG),  # too small
+    (dict(ws=A + 2 * GAP), fa.FA_ERR_INVALID_ARG),             # overlaps V
+    (dict(Q=0), fa.FA_ERR_INVALID_ARG),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+])
+def test_naive_host_side_rejections(lib, kwargs, expect):
+    assert naive_call(lib, **kwargs) == expect
