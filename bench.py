@@ -399,6 +399,41 @@ def run_native(args):
     if st != fa.FA_OK:
         raise RuntimeError(f"device status after timed steps: {fa.fa_status_string(st)} {info}")
 
+    # The standard-attention comparator on the same inputs: S and P in HBM
+    # ("01 · 注意力为什么是 IO 瓶颈" §3), same timing rules as the fused steps.
+    comparator = None
+    if not args.no_comparator:
+        ws_bytes = fa.fa_naive_workspace_bytes(B, H, N)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+        o_n = torch.empty_like(qd)
+        lse_n = torch.empty_like(lse)
+        for _ in range(args.warmup):
+            fa.fa_naive_fwd(qd, kd, vd, o_n, lse_n, scale, ws)
+        torch.cuda.synchronize(device)
+        n_steps = max(3, min(args.steps, 20))
+        cs = [torch.cuda.Event(enable_timing=True) for _ in range(n_steps)]
+        ce = [torch.cuda.Event(enable_timing=True) for _ in range(n_steps)]
+        for i in range(n_steps):
+            flush.fill_(float(i))
+            cs[i].record(stream)
+            fa.fa_naive_fwd(qd, kd, vd, o_n, lse_n, scale, ws)
+            ce[i].record(stream)
+        torch.cuda.synchronize(device)
+        st, info = fa.fa_get_device_status()
+        if st != fa.FA_OK:
+            raise RuntimeError(f"device status after the comparator: {fa.fa_status_string(st)} {info}")
+        naive_ms = sum(a.elapsed_time(b) for a, b in zip(cs, ce)) / n_steps
+        fused_ms = sum(step_ms) / len(step_ms)
+        comparator = {
+            "impl": "standard attention: S = QK^T, P = softmax(S) and O = PV as 3 launches, S/P in HBM (bf16)",
+            "steps": n_steps, "ms_per_step": naive_ms, "value": flops / (naive_ms * 1e-3) / 1e12, "unit": UNIT,
+            "speedup_of_fused": naive_ms / fused_ms,
+            "workspace_bytes": ws_bytes, "fused_workspace_bytes": 0,
+            "max_abs_diff_O_vs_fused": float((o_n.float() - o.float()).abs().max()),
+        }
+        del ws, o_n, lse_n
+        torch.cuda.empty_cache()
+
     # end to end through the public API: pinned host inputs in, O and LSE back out
     qh, kh, vh = (x.pin_memory() for x in (q, k, v))
     oh = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
@@ -448,6 +483,8 @@ def run_native(args):
             "clocks": clocks.summary(),
             "step_ms": {"min": min(step_ms), "median": statistics.median(step_ms), "max": max(step_ms)},
         }
+        if comparator is not None:
+            line["comparator"] = comparator
         if cpu is not None:
             line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)
@@ -467,6 +504,7 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU oracle sample size (seconds of work)")
     ap.add_argument("--ref-step-s", type=float, default=2.0, help="reference arm: seconds of oracle work per step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-comparator", action="store_true", help="skip timing standard attention (S/P in HBM)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
