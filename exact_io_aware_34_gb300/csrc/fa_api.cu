@@ -18,6 +18,15 @@
 #include "fa_fwd_kernel.cuh"
 #include "naive_kernels.cuh"
 
+// Device scratch for fa_naive_fwd_noalloc: the score/probability matrices of
+// the standard-attention path live here instead of in caller memory. It is
+// part of this library's device image, so every GPU that loads the library
+// holds these 64 MiB until the process exits. In host code the name below is
+// only a host-side stand-in; its device address comes from
+// cudaGetSymbolAddress (see naive_static_scratch()).
+static constexpr size_t kNaiveStaticScratchBytes = 64ull << 20;
+static __device__ __align__(256) unsigned char g_naive_static_scratch[kNaiveStaticScratchBytes];
+
 namespace {
 
 thread_local int t_last_cuda_error = 0;
@@ -220,6 +229,17 @@ fa_status_t check_args(const void* Q, const void* K, const void* V, const void* 
   return FA_OK;
 }
 
+// Device address of g_naive_static_scratch on the current device, looked up
+// once per device (the first fa_naive_fwd_noalloc call on that device).
+cudaError_t naive_static_scratch(int dev, void** out) {
+  static std::once_flag once[64];
+  static void* addr[64];
+  static cudaError_t err[64];
+  std::call_once(once[dev], [&] { err[dev] = cudaGetSymbolAddress(&addr[dev], g_naive_static_scratch); });
+  *out = addr[dev];
+  return err[dev];
+}
+
 // A correct pipeline never waits anywhere near this long; it only bounds
 // how long a broken one can hold the GPU.
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
@@ -280,6 +300,22 @@ fa_status_t fa_naive_fwd(const void* Q, const void* K, const void* V, void* O, f
   if (overlaps(workspace, need, LSE, n_lse)) return FA_ERR_INVALID_ARG;
   if (d == 64) return naive_launch<64>(Q, K, V, O, LSE, B, H, N, scale, workspace, stream);
   return naive_launch<128>(Q, K, V, O, LSE, B, H, N, scale, workspace, stream);
+}
+
+fa_status_t fa_naive_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+                                 int N, int d, float scale, cudaStream_t stream) {
+  fa_status_t st = check_args(Q, K, V, O, LSE, B, H, N, d, scale);
+  if (st != FA_OK) return st;
+  if (fa_naive_workspace_bytes(B, H, N) > kNaiveStaticScratchBytes) return FA_ERR_UNSUPPORTED;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= 64) return FA_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  e = naive_static_scratch(dev, &scratch);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (d == 64) return naive_launch<64>(Q, K, V, O, LSE, B, H, N, scale, scratch, stream);
+  return naive_launch<128>(Q, K, V, O, LSE, B, H, N, scale, scratch, stream);
 }
 
 const char* fa_status_string(fa_status_t status) {

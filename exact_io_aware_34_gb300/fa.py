@@ -25,7 +25,7 @@ FA_ERR_TIMEOUT = 4
 
 #: every symbol include/fa.h declares
 EXPORTED = ("fa_fwd", "fa_get_device_status", "fa_status_string", "fa_last_cuda_error", "fa_fwd_fault_test",
-            "fa_naive_fwd", "fa_naive_workspace_bytes")
+            "fa_naive_fwd", "fa_naive_workspace_bytes", "fa_naive_fwd_noalloc")
 
 _lib = None
 
@@ -62,6 +62,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_naive_workspace_bytes.restype = ctypes.c_size_t
     lib.fa_naive_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, vp, ctypes.c_size_t, vp]
     lib.fa_naive_fwd.restype = i
+    lib.fa_naive_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, vp]
+    lib.fa_naive_fwd_noalloc.restype = i
     _lib = lib
     return lib
 

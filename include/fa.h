@@ -115,6 +115,30 @@ fa_status_t fa_naive_fwd(const void* Q, const void* K, const void* V, void* O, f
                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * fa_naive_fwd_noalloc -- fa_naive_fwd for callers that cannot allocate
+ * device memory, e.g. a service that reserves all of its GPU memory at
+ * start-up and forbids any later cudaMalloc, or a code path where the latency
+ * or possible failure of an allocation is not acceptable. (The pages have no
+ * counterpart: this is an interface convenience of this library.)
+ * Same arguments, results and errors as fa_naive_fwd, minus the workspace:
+ * the N x N matrices live in a 64 MiB (67108864-byte) array inside the
+ * library's device image, which every GPU that loads the library holds until
+ * the process exits. Requests whose fa_naive_workspace_bytes() exceed
+ * 64 MiB return FA_ERR_UNSUPPORTED without launching anything (for example
+ * B*H = 8 heads of N = 2048, or one head of N = 5760, still fit).
+ *   - The call allocates nothing (no cudaMalloc, no library allocator).
+ *   - The first call on a device looks the array's device address up
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array, and the array keeps the
+ *     last call's contents (nothing in it needs to start at zero). Calls whose
+ *     kernels overlap on the GPU (different streams, no ordering between them)
+ *     race on it: order them, e.g. issue them on one stream.
+ */
+fa_status_t fa_naive_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                                 int B, int H, int N, int d, float scale, cudaStream_t stream);
+
+/*
  * fa_fwd_fault_test -- TEST HOOK, not for production use. Same as fa_fwd,
  * but (a) every device-side wait gives up after `timeout_ns` nanoseconds,
  * and (b) when `drop_load` >= 0 the producer skips the drop_load-th K/V tile
