@@ -8,3 +8,9 @@ from .attention import (  # noqa: F401
     naive_bf16_attention,
     safe_softmax,
 )
+from .backward import (  # noqa: F401
+    attention_bwd,
+    attention_bwd_heads,
+    attention_bwd_recompute,
+    naive_bf16_attention_bwd,
+)
