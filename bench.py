@@ -14,6 +14,9 @@ region; the max over ranks of the summed device time. For N > 1 (launched by
 torchrun) every rank runs its own copy of the workload (independent problems,
 no collective on the data path): weak scaling.
 
+The same run also times the backward pass (fa_bwd, three launches) on the
+same workload and reports it under "bwd" (skip with --no-bwd).
+
 --impl reference times the CPU oracle (float64, numpy) on the host cores, on a
 bounded sample of the same workload per step.
 """
@@ -434,6 +437,49 @@ def run_native(args):
         del ws, o_n, lse_n
         torch.cuda.empty_cache()
 
+    # The backward pass by recomputation on the same workload (O and LSE from the
+    # forward above, dO seeded), same timing rules: flush before every step,
+    # events on the launching stream, clocks sampled during the timed steps.
+    bwd = None
+    if not args.no_bwd:
+        do = inputs.make_grad(B, H, N, d, w.seed).to(device)
+        dq, dk, dv = (torch.empty_like(qd) for _ in range(3))
+        ws_b = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N), dtype=torch.uint8, device=device)
+        for _ in range(args.warmup):
+            fa.fa_bwd(qd, kd, vd, o, do, lse, dq, dk, dv, scale, ws_b)
+        torch.cuda.synchronize(device)
+        st, info = fa.fa_get_device_status()
+        if st != fa.FA_OK:
+            raise RuntimeError(f"device status after backward warm-up: {fa.fa_status_string(st)} {info}")
+        n_steps = max(3, min(args.steps, 20))
+        bs = [torch.cuda.Event(enable_timing=True) for _ in range(n_steps)]
+        be = [torch.cuda.Event(enable_timing=True) for _ in range(n_steps)]
+        with ClockSampler(local, uuid) as bclocks:
+            for i in range(n_steps):
+                flush.fill_(float(i))
+                bs[i].record(stream)
+                fa.fa_bwd(qd, kd, vd, o, do, lse, dq, dk, dv, scale, ws_b)
+                be[i].record(stream)
+            torch.cuda.synchronize(device)
+        st, info = fa.fa_get_device_status()
+        if st != fa.FA_OK:
+            raise RuntimeError(f"device status after backward steps: {fa.fa_status_string(st)} {info}")
+        b_ms = [a.elapsed_time(b) for a, b in zip(bs, be)]
+        bwd_ms = sum(b_ms) / n_steps
+        bwd_flops = 2.5 * flops          # five N x N x d products per head: 10*B*H*N^2*d
+        bwd = {
+            "metric": "attention bwd TFLOP/s (10·B·H·N²·d: the five N×N×d products of the gradient)",
+            "value": bwd_flops / (bwd_ms * 1e-3) / 1e12, "unit": UNIT, "steps": n_steps,
+            "ms_per_step": bwd_ms,
+            "step_ms": {"min": min(b_ms), "median": statistics.median(b_ms), "max": max(b_ms)},
+            "executed_tflops": 3.5 * flops / (bwd_ms * 1e-3) / 1e12,   # S and dP formed in both kernels
+            "gpu_launches": 3 * n_steps,
+            "workspace_bytes": ws_b.numel(),
+            "clocks": bclocks.summary(),
+        }
+        del do, dq, dk, dv, ws_b
+        torch.cuda.empty_cache()
+
     # end to end through the public API: pinned host inputs in, O and LSE back out
     qh, kh, vh = (x.pin_memory() for x in (q, k, v))
     oh = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
@@ -485,6 +531,12 @@ def run_native(args):
         }
         if comparator is not None:
             line["comparator"] = comparator
+        if bwd is not None:
+            bwd["roofline"] = {"bound": "tensor", "achieved": bwd["value"], "peak": peaks["bf16_tflops"],
+                               "unit": UNIT, "frac": bwd["value"] / peaks["bf16_tflops"], "traffic": None,
+                               "peak_source": f"{peak_src} dense bf16 burst",
+                               "kernels": "bwd_prep_kernel, fa_bwd_dq_kernel<%d>, fa_bwd_dkdv_kernel<%d>" % (d, d)}
+            line["bwd"] = bwd
         if cpu is not None:
             line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)
@@ -505,6 +557,7 @@ def main(argv=None):
     ap.add_argument("--ref-step-s", type=float, default=2.0, help="reference arm: seconds of oracle work per step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-comparator", action="store_true", help="skip timing standard attention (S/P in HBM)")
+    ap.add_argument("--no-bwd", action="store_true", help="skip timing the backward pass")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "../../include/fa.h"
+#include "fa_bwd_kernel.cuh"
 #include "fa_fwd_kernel.cuh"
 #include "naive_kernels.cuh"
 
@@ -244,6 +245,71 @@ cudaError_t naive_static_scratch(int dev, void** out) {
 // how long a broken one can hold the GPU.
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
 
+// ---------------------------------------------------------------- backward
+// Query rows per head in the backward workspace: N rounded up to whole
+// 128-row blocks, so that every block's slice starts 512-byte aligned.
+inline long long bwd_npad(int N) { return (static_cast<long long>(N) + 127) / 128 * 128; }
+
+template <int HD>
+fa_status_t bwd_launch(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
+                       void* dQ, void* dK, void* dV, int B, int H, int N, float scale, void* ws,
+                       cudaStream_t stream) {
+  using C = fa::BwdCfg<HD>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= 64) return FA_ERR_UNSUPPORTED;
+  static std::once_flag once[64];
+  static cudaError_t attr_err[64];
+  std::call_once(once[dev], [&] {
+    attr_err[dev] = cudaFuncSetAttribute(fa::fa_bwd_dq_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (attr_err[dev] == cudaSuccess)
+      attr_err[dev] = cudaFuncSetAttribute(fa::fa_bwd_dkdv_kernel<HD>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  });
+  if (attr_err[dev] != cudaSuccess) return cuda_fail(attr_err[dev]);
+
+  const int BH = B * H;
+  CUtensorMap mq, mk, mv, mdo;
+  if (!make_map(&mq, Q, BH, N, HD) || !make_map(&mk, K, BH, N, HD) || !make_map(&mv, V, BH, N, HD) ||
+      !make_map(&mdo, dO, BH, N, HD))
+    return cuda_fail(cudaErrorInvalidValue);
+
+  const long long npad = bwd_npad(N);
+  const long long rows = static_cast<long long>(BH) * npad;
+  fa::BwdParams p;
+  p.dQ = static_cast<__nv_bfloat16*>(dQ);
+  p.dK = static_cast<__nv_bfloat16*>(dK);
+  p.dV = static_cast<__nv_bfloat16*>(dV);
+  p.nlse2 = static_cast<const float*>(ws);
+  p.ndelta = static_cast<const float*>(ws) + rows;
+  p.N = N;
+  p.Npad = static_cast<int>(npad);
+  p.H = H;
+  p.n_blocks = static_cast<int>(npad / C::kBlk);
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  p.scale = scale;
+  p.timeout_ns = kDefaultTimeoutNs;
+
+  // 1. -LSE*log2(e) and -D per query row (one warp each, 8 per block)
+  fa::bwd_prep_kernel<HD><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), LSE, static_cast<float*>(ws),
+      static_cast<float*>(ws) + rows, N, p.Npad, rows);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  const dim3 grid(static_cast<unsigned>(p.n_blocks), H, B);
+  // 2. dQ, one CTA per 128 query rows
+  fa::fa_bwd_dq_kernel<HD><<<grid, C::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  // 3. dK and dV, one CTA per 128 key rows
+  fa::fa_bwd_dkdv_kernel<HD><<<grid, C::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -316,6 +382,40 @@ fa_status_t fa_naive_fwd_noalloc(const void* Q, const void* K, const void* V, vo
   if (e != cudaSuccess) return cuda_fail(e);
   if (d == 64) return naive_launch<64>(Q, K, V, O, LSE, B, H, N, scale, scratch, stream);
   return naive_launch<128>(Q, K, V, O, LSE, B, H, N, scale, scratch, stream);
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int N) {
+  if (B < 1 || H < 1 || N < 1) return 0;
+  return 2 * static_cast<size_t>(B) * H * static_cast<size_t>(bwd_npad(N)) * 4;
+}
+
+fa_status_t fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
+                   void* dQ, void* dK, void* dV, int B, int H, int N, int d, float scale, void* workspace,
+                   size_t workspace_bytes, cudaStream_t stream) {
+  fa_status_t st = check_args(Q, K, V, O, LSE, B, H, N, d, scale);
+  if (st != FA_OK) return st;
+  if (!dO || !dQ || !dK || !dV || !workspace) return FA_ERR_INVALID_ARG;
+  for (const void* ptr : {dO, static_cast<const void*>(dQ), static_cast<const void*>(dK),
+                          static_cast<const void*>(dV)})
+    if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return FA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) % 128 != 0) return FA_ERR_INVALID_ARG;
+  const size_t need = fa_bwd_workspace_bytes(B, H, N);
+  if (workspace_bytes < need) return FA_ERR_INVALID_ARG;
+  const size_t n_qkv = static_cast<size_t>(B) * H * N * d * 2;
+  const size_t n_lse = static_cast<size_t>(B) * H * N * 4;
+  // Every written buffer (dQ, dK, dV, workspace) is disjoint from every
+  // input and from the other written buffers.
+  const void* outs[4] = {dQ, dK, dV, workspace};
+  const size_t out_n[4] = {n_qkv, n_qkv, n_qkv, need};
+  for (int a = 0; a < 4; ++a) {
+    for (const void* in : {Q, K, V, O, dO})
+      if (overlaps(outs[a], out_n[a], in, n_qkv)) return FA_ERR_INVALID_ARG;
+    if (overlaps(outs[a], out_n[a], LSE, n_lse)) return FA_ERR_INVALID_ARG;
+    for (int b = a + 1; b < 4; ++b)
+      if (overlaps(outs[a], out_n[a], outs[b], out_n[b])) return FA_ERR_INVALID_ARG;
+  }
+  if (d == 64) return bwd_launch<64>(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, scale, workspace, stream);
+  return bwd_launch<128>(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, scale, workspace, stream);
 }
 
 const char* fa_status_string(fa_status_t status) {

@@ -1,0 +1,636 @@
+// Exact-attention backward kernels for sm_103a (tcgen05 + TMEM + TMA).
+//
+// What is computed: the gradients of <dO, O> for O = softmax(scale Q K^T) V,
+// with the probabilities rebuilt from the forward's per-row LSE rather than
+// read back ("01 · 注意力为什么是 IO 瓶颈" §7: the fused method keeps only O
+// and LSE for the backward and recomputes P from them). Per (b, h):
+//   P  = exp(scale Q K^T - LSE)        dV = P^T dO
+//   dP = dO V^T                         dS = P * (dP - D),  D_i = dO_i . O_i
+//   dQ = scale dS K                     dK = scale dS^T Q
+//
+// Three launches on the caller's stream:
+//   bwd_prep_kernel     per query row: -D and -LSE*log2(e) into a workspace
+//                       whose rows are padded to a multiple of 128; padding
+//                       rows get 0 and -inf, so their probabilities are zero.
+//   fa_bwd_dq_kernel    one CTA per 128 query rows of one (b, h), streaming
+//                       the K/V blocks: S = Q K_j^T, dP = dO V_j^T, dS,
+//                       dQ += dS K_j.
+//   fa_bwd_dkdv_kernel  one CTA per 128 key rows of one (b, h), streaming the
+//                       Q/dO blocks: S^T = K Q_i^T, dP^T = V dO_i^T, P^T,
+//                       dS^T, dV += P^T dO_i, dK += dS^T Q_i.
+// S and dP are formed in both kernels (7 tile products per pair of blocks
+// instead of 5). In exchange every accumulator stays in the TMEM of the one
+// CTA that owns it: no atomics, a deterministic result, and the state fits
+// TMEM (512 columns): the key-block owner holds dV and dK (2 x d columns)
+// plus two 128-column score regions.
+//
+// The two score regions R0, R1 alternate: block i's S goes to R[i&1] and its
+// dP to R[(i+1)&1]. Once the softmax warps have loaded both, the MMA warp
+// issues block i+1's S into R[(i+1)&1] while the softmax warps compute; they
+// write the packed bf16 results (P and dS, or dS alone) over S_i in R[i&1].
+// The tile products of block i that read those results, then block i+1's dP
+// (into R[i&1]), follow in issue order, which the tensor core keeps.
+//
+// Warp roles (10 warps, as in the forward kernel):
+//   warps 0-7  elementwise step + epilogue: warp w serves TMEM lane quarter
+//              w & 3 (32 rows) and the 64 streamed-block columns
+//              [64 (w >> 2), 64 (w >> 2) + 64)
+//   warp 8     TMA producer (one thread)
+//   warp 9     TMEM allocator and MMA issuer (one thread)
+// Packed bf16 results of warp half h live in that half's own score columns
+// [64h, 64h + 32) (and dS of the key-block kernel in [64h + 32, 64h + 64)),
+// so that no warp overwrites scores another warp has yet to load. For the
+// tile products that read them, key step kk (16 streamed rows) sits at
+// column 64 (kk >> 2) + 8 (kk & 3).
+#pragma once
+
+#include "fa_fwd_kernel.cuh"
+
+namespace fa {
+
+enum : unsigned int {
+  kRoleDqProducer = 4, kRoleDqMma = 5, kRoleDqSoftmax = 6,
+  kRoleDkvProducer = 7, kRoleDkvMma = 8, kRoleDkvSoftmax = 9,
+};
+
+template <int HD>
+struct BwdCfg {
+  static constexpr int kBlk = 128;                 // rows per block, both directions
+  static constexpr int kChunks = HD / 64;          // 128-byte swizzle chunks per row
+  static constexpr int kChunkBytes = 128 * 128;    // 128 rows x 128 bytes
+  static constexpr int kTileBytes = kChunks * kChunkBytes;
+  static constexpr int kPairBytes = 2 * kTileBytes;            // (Q_i, dO_i) or (K_j, V_j)
+  static constexpr int kStages = (HD == 128) ? 2 : 4;          // ring slots of pairs
+  static constexpr int kVecBytes = 2 * 128 * 4;                // -LSE*log2e and -D of 128 rows
+  static constexpr int kSmemBytes = kPairBytes + kStages * kPairBytes + kStages * kVecBytes + 1024;
+  static constexpr int kThreads = 320;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(128, 128, false, false);
+  static constexpr uint32_t kIdescAcc = ptx::idesc_bf16_f32(128, HD, false, true);
+};
+
+struct BwdParams {
+  __nv_bfloat16* dQ;
+  __nv_bfloat16* dK;
+  __nv_bfloat16* dV;
+  const float* nlse2;     // [B*H][Npad]: -LSE * log2(e); -inf on padding rows
+  const float* ndelta;    // [B*H][Npad]: -D; 0 on padding rows
+  int N;
+  int Npad;               // N rounded up to a multiple of 128
+  int H;
+  int n_blocks;           // Npad / 128
+  float scale_log2;       // scale * log2(e)
+  float scale;
+  unsigned long long timeout_ns;
+};
+
+// ---------------------------------------------------------------- prep
+// One warp per padded query row: D = dO_r . O_r (float32 sum of the exact
+// products of bf16 values) and LSE_r * log2(e), stored negated.
+template <int HD>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ O,
+                                                       const __nv_bfloat16* __restrict__ dO,
+                                                       const float* __restrict__ LSE, float* __restrict__ nlse2,
+                                                       float* __restrict__ ndelta, int N, int Npad,
+                                                       long long rows) {
+  const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (gw >= rows) return;
+  const long long bh = gw / Npad;
+  const int r = static_cast<int>(gw - bh * Npad);
+  float dsum = 0.f;
+  float nl = -INFINITY;
+  if (r < N) {
+    constexpr int kPer = HD / 32;     // elements per lane: 4 (8 bytes) or 2 (4 bytes)
+    const size_t off = (static_cast<size_t>(bh) * N + r) * HD + lane * kPer;
+    __nv_bfloat162 o2[kPer / 2], g2[kPer / 2];
+    if constexpr (kPer == 4) {
+      const uint2 a = *reinterpret_cast<const uint2*>(O + off);
+      const uint2 b = *reinterpret_cast<const uint2*>(dO + off);
+      o2[0] = *reinterpret_cast<const __nv_bfloat162*>(&a.x);
+      o2[1] = *reinterpret_cast<const __nv_bfloat162*>(&a.y);
+      g2[0] = *reinterpret_cast<const __nv_bfloat162*>(&b.x);
+      g2[1] = *reinterpret_cast<const __nv_bfloat162*>(&b.y);
+    } else {
+      o2[0] = *reinterpret_cast<const __nv_bfloat162*>(O + off);
+      g2[0] = *reinterpret_cast<const __nv_bfloat162*>(dO + off);
+    }
+#pragma unroll
+    for (int e = 0; e < kPer / 2; ++e) {
+      const float2 of = __bfloat1622float2(o2[e]);
+      const float2 gf = __bfloat1622float2(g2[e]);
+      dsum = fmaf(of.x, gf.x, dsum);
+      dsum = fmaf(of.y, gf.y, dsum);
+    }
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, s);
+    nl = -LSE[static_cast<size_t>(bh) * N + r] * 1.4426950408889634074f;
+  }
+  if (lane == 0) {
+    nlse2[gw] = nl;
+    ndelta[gw] = -dsum;
+  }
+}
+
+// S-shaped product over the model dimension: D[128 x 128] = A B^T with A and
+// B two 128-row tiles in the K-major swizzled layout (k = 0 .. HD).
+template <int HD>
+__device__ __forceinline__ void issue_tile_qk(uint32_t d_tmem, uint32_t a_tile, uint32_t b_tile) {
+  using C = BwdCfg<HD>;
+#pragma unroll
+  for (int kk = 0; kk < HD / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+    ptx::mma_ss(d_tmem, ptx::desc_kmajor_sw128(a_tile + off), ptx::desc_kmajor_sw128(b_tile + off), C::kIdescS,
+                kk > 0 ? 1u : 0u);
+  }
+}
+
+// Accumulating product over the 128 streamed rows: D[128 x HD] += A B with A
+// packed bf16 in TMEM (the layout described at the top of this file, base
+// column a_col) and B a 128 x HD tile read MN-major from shared memory.
+template <int HD>
+__device__ __forceinline__ void issue_tile_acc(uint32_t d_tmem, uint32_t a_col, uint32_t b_tile, bool accumulate) {
+  using C = BwdCfg<HD>;
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint64_t b_desc = ptx::desc_mnmajor_sw128(b_tile + kk * 16 * 128, C::kChunkBytes);
+    ptx::mma_ts(d_tmem, a_col + 64 * (kk >> 2) + 8 * (kk & 3), b_desc, C::kIdescAcc,
+                (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+// Epilogue helper: 32 accumulator columns of this thread's row, times `mul`,
+// to bf16 at dst (64 bytes, 16-byte aligned) when `store`.
+__device__ __forceinline__ void store_row32(uint32_t taddr, float mul, __nv_bfloat16* dst, bool store) {
+  uint32_t v[32];
+  ptx::tmem_ld32(taddr, v);
+  ptx::tmem_ld_wait();
+  ptx::reg_fence32(v);
+  uint32_t packed[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    packed[i] = ptx::pack_bf16x2(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
+  if (store) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      d4[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+  }
+}
+
+// ---------------------------------------------------------------- dQ
+template <int HD>
+__global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
+    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                     const BwdParams p) {
+  using C = BwdCfg<HD>;
+  constexpr uint32_t kColDQ = 0;
+  constexpr uint32_t kColR = HD;    // R0 = kColR, R1 = kColR + 128
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_in_full;
+  __shared__ __align__(8) uint64_t bar_kv_full[C::kStages];
+  __shared__ __align__(8) uint64_t bar_kv_empty[C::kStages];
+  __shared__ __align__(8) uint64_t bar_s_full;
+  __shared__ __align__(8) uint64_t bar_dp_free;
+  __shared__ __align__(8) uint64_t bar_p_full;
+  __shared__ __align__(8) uint64_t bar_acc_full;
+  __shared__ __align__(8) uint64_t bar_drain;
+  __shared__ uint32_t tmem_base_slot;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bh = blockIdx.z * p.H + blockIdx.y;
+  const int q0 = blockIdx.x * C::kBlk;
+  const int n = p.n_blocks;
+
+  const uint32_t smem_base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sQ = smem_base;
+  const uint32_t sdO = smem_base + C::kTileBytes;
+  const uint32_t sRing = smem_base + C::kPairBytes;    // slot s: K_j at s * pair, V_j at s * pair + tile
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_u32(&bar_in_full), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&bar_kv_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bar_kv_empty[s]), 1);
+    }
+    ptx::mbar_init(ptx::smem_u32(&bar_s_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&bar_dp_free), 256);
+    ptx::mbar_init(ptx::smem_u32(&bar_p_full), 256);
+    ptx::mbar_init(ptx::smem_u32(&bar_acc_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&bar_drain), 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 9) {
+    ptx::tmem_alloc(ptx::smem_u32(&tmem_base_slot), C::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (warp == 8 && lane == 0) {
+    ptx::prefetch_tmap(&tmQ);
+    ptx::prefetch_tmap(&tmK);
+    ptx::prefetch_tmap(&tmV);
+    ptx::prefetch_tmap(&tmdO);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = tmem_base_slot;
+  volatile int* abort_ptr = &abort_flag;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_once = ptx::policy_evict_first();
+      const uint64_t pol_shared = ptx::policy_evict_last();
+      const uint32_t in_full = ptx::smem_u32(&bar_in_full);
+      ptx::mbar_arrive_expect_tx(in_full, C::kPairBytes);
+      for (int c = 0; c < C::kChunks; ++c) {
+        ptx::tma_load_3d(sQ + c * C::kChunkBytes, &tmQ, in_full, c * 64, q0, bh, pol_once);
+        ptx::tma_load_3d(sdO + c * C::kChunkBytes, &tmdO, in_full, c * 64, q0, bh, pol_once);
+      }
+      int issued = 0;
+      bool ok = true;
+      for (int j = 0; j < n; ++j) {
+        const int slot = j % C::kStages;
+        if (!wait_or_abort(ptx::smem_u32(&bar_kv_empty[slot]), ((j / C::kStages) & 1) ^ 1u, abort_ptr,
+                           p.timeout_ns, kRoleDqProducer)) {
+          ok = false;
+          break;
+        }
+        issued = j + 1;
+        const uint32_t full = ptx::smem_u32(&bar_kv_full[slot]);
+        const uint32_t dst = sRing + slot * C::kPairBytes;
+        ptx::mbar_arrive_expect_tx(full, C::kPairBytes);
+        for (int c = 0; c < C::kChunks; ++c) {
+          ptx::tma_load_3d(dst + c * C::kChunkBytes, &tmK, full, c * 64, j * C::kBlk, bh, pol_shared);
+          ptx::tma_load_3d(dst + C::kTileBytes + c * C::kChunkBytes, &tmV, full, c * 64, j * C::kBlk, bh,
+                           pol_shared);
+        }
+      }
+      if (!ok || *abort_ptr) {
+        drain_wait(in_full, 0, p.timeout_ns);
+        for (int j = issued > C::kStages ? issued - C::kStages : 0; j < issued; ++j)
+          drain_wait(ptx::smem_u32(&bar_kv_full[j % C::kStages]), (j / C::kStages) & 1, p.timeout_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      auto region = [&](int j) { return tmem_base + kColR + 128u * static_cast<uint32_t>(j & 1); };
+      auto k_tile = [&](int j) { return sRing + (j % C::kStages) * C::kPairBytes; };
+      bool ok = wait_or_abort(ptx::smem_u32(&bar_in_full), 0, abort_ptr, p.timeout_ns, kRoleDqMma);
+      if (ok) ok = wait_or_abort(ptx::smem_u32(&bar_kv_full[0]), 0, abort_ptr, p.timeout_ns, kRoleDqMma);
+      if (ok) {
+        ptx::tc_fence_after();
+        issue_tile_qk<HD>(region(0), sQ, k_tile(0));                   // S_0 = Q K_0^T
+        issue_tile_qk<HD>(region(1), sdO, k_tile(0) + C::kTileBytes);  // dP_0 = dO V_0^T
+        ptx::mma_commit(ptx::smem_u32(&bar_s_full));
+      }
+      for (int j = 0; j < n && ok; ++j) {
+        if (j + 1 < n) {
+          const int s1 = (j + 1) % C::kStages;
+          ok = wait_or_abort(ptx::smem_u32(&bar_kv_full[s1]), ((j + 1) / C::kStages) & 1, abort_ptr, p.timeout_ns,
+                             kRoleDqMma);
+          if (!ok) break;
+          ok = wait_or_abort(ptx::smem_u32(&bar_dp_free), j & 1, abort_ptr, p.timeout_ns, kRoleDqMma);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          issue_tile_qk<HD>(region(j + 1), sQ, k_tile(j + 1));          // S_{j+1}
+        }
+        ok = wait_or_abort(ptx::smem_u32(&bar_p_full), j & 1, abort_ptr, p.timeout_ns, kRoleDqMma);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        issue_tile_acc<HD>(tmem_base + kColDQ, region(j), k_tile(j), j > 0);   // dQ += dS_j K_j
+        ptx::mma_commit(ptx::smem_u32(&bar_kv_empty[j % C::kStages]));
+        if (j + 1 < n) {
+          issue_tile_qk<HD>(region(j), sdO, k_tile(j + 1) + C::kTileBytes);   // dP_{j+1}
+          ptx::mma_commit(ptx::smem_u32(&bar_s_full));
+        }
+      }
+      if (ok) {
+        ptx::mma_commit(ptx::smem_u32(&bar_acc_full));
+      } else {
+        ptx::mma_commit(ptx::smem_u32(&bar_drain));
+        drain_wait(ptx::smem_u32(&bar_drain), 0, p.timeout_ns);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ dS + epilogue
+    const int quarter = warp & 3;
+    const int half = warp >> 2;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    const size_t vrow = static_cast<size_t>(bh) * p.Npad + q0 + row;
+    const float nl = p.nlse2[vrow];
+    const float nd = p.ndelta[vrow];
+    const uint64_t sl2x2 = ptx::f2_pack(p.scale_log2, p.scale_log2);
+    const uint64_t nlx2 = ptx::f2_pack(nl, nl);
+    const uint64_t ndx2 = ptx::f2_pack(nd, nd);
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      ok = wait_warp_or_abort(ptx::smem_u32(&bar_s_full), j & 1, abort_ptr, p.timeout_ns, kRoleDqSoftmax);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const uint32_t tS = tmem_base + lane_addr + kColR + 128u * (j & 1) + 64u * half;
+      const uint32_t tP = tmem_base + lane_addr + kColR + 128u * ((j + 1) & 1) + 64u * half;
+      uint32_t s[2][32], dp[2][32];
+      ptx::tmem_ld32(tS, s[0]);
+      ptx::tmem_ld32(tS + 32, s[1]);
+      ptx::tmem_ld32(tP, dp[0]);
+      ptx::tmem_ld32(tP + 32, dp[1]);
+      ptx::tmem_ld_wait();
+      ptx::reg_fence32(s[0]);
+      ptx::reg_fence32(s[1]);
+      ptx::reg_fence32(dp[0]);
+      ptx::reg_fence32(dp[1]);
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(ptx::smem_u32(&bar_dp_free));
+
+      const int valid = p.N - j * C::kBlk - 64 * half;   // keys of this warp's 64 that exist
+      const bool ragged = valid < 64;
+      uint32_t pds[32];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          float x0, x1;
+          ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[c][2 * k]), __uint_as_float(s[c][2 * k + 1])),
+                                     sl2x2, nlx2),
+                         x0, x1);
+          float p0 = ptx::ex2_approx(x0);
+          float p1 = ptx::ex2_approx(x1);
+          if (ragged) {   // keys past N: exact zeros whatever the fill gave
+            if (32 * c + 2 * k >= valid) p0 = 0.f;
+            if (32 * c + 2 * k + 1 >= valid) p1 = 0.f;
+          }
+          const uint64_t t =
+              ptx::f2_add(ptx::f2_pack(__uint_as_float(dp[c][2 * k]), __uint_as_float(dp[c][2 * k + 1])), ndx2);
+          float d0, d1;
+          ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(p0, p1), t), d0, d1);
+          pds[16 * c + k] = ptx::pack_bf16x2(d0, d1);
+        }
+      }
+      ptx::tmem_st32(tS, pds);
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(ptx::smem_u32(&bar_p_full));
+    }
+    if (ok) ok = wait_warp_or_abort(ptx::smem_u32(&bar_acc_full), 0, abort_ptr, p.timeout_ns, kRoleDqSoftmax);
+    if (ok) {
+      ptx::tc_fence_after();
+      const int q = q0 + row;
+      __nv_bfloat16* dst = p.dQ + (static_cast<size_t>(bh) * p.N + q) * HD + half * (HD / 2);
+#pragma unroll
+      for (int c = 0; c < HD / 64; ++c)
+        store_row32(tmem_base + lane_addr + kColDQ + half * (HD / 2) + 32 * c, p.scale, dst + 32 * c, q < p.N);
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- dK, dV
+template <int HD>
+__global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
+    fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                       const BwdParams p) {
+  using C = BwdCfg<HD>;
+  constexpr uint32_t kColDV = 0;
+  constexpr uint32_t kColDK = HD;
+  constexpr uint32_t kColR = 2 * HD;    // R0 = kColR, R1 = kColR + 128
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_kv_full;
+  __shared__ __align__(8) uint64_t bar_in_full[C::kStages];
+  __shared__ __align__(8) uint64_t bar_in_empty[C::kStages];
+  __shared__ __align__(8) uint64_t bar_s_full;
+  __shared__ __align__(8) uint64_t bar_dp_free;
+  __shared__ __align__(8) uint64_t bar_p_full;
+  __shared__ __align__(8) uint64_t bar_acc_full;
+  __shared__ __align__(8) uint64_t bar_drain;
+  __shared__ uint32_t tmem_base_slot;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bh = blockIdx.z * p.H + blockIdx.y;
+  const int kv0 = blockIdx.x * C::kBlk;
+  const int n = p.n_blocks;
+
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t smem_base = (raw + 1023u) & ~1023u;
+  const uint32_t sK = smem_base;
+  const uint32_t sV = smem_base + C::kTileBytes;
+  const uint32_t sRing = smem_base + C::kPairBytes;                  // slot s: Q_i, then dO_i
+  const uint32_t sVec = sRing + C::kStages * C::kPairBytes;          // slot s: [-lse2 x 128][-D x 128]
+  const float* vec = reinterpret_cast<const float*>(smem_raw + (sVec - raw));
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_u32(&bar_kv_full), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&bar_in_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bar_in_empty[s]), 1);
+    }
+    ptx::mbar_init(ptx::smem_u32(&bar_s_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&bar_dp_free), 256);
+    ptx::mbar_init(ptx::smem_u32(&bar_p_full), 256);
+    ptx::mbar_init(ptx::smem_u32(&bar_acc_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&bar_drain), 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 9) {
+    ptx::tmem_alloc(ptx::smem_u32(&tmem_base_slot), C::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (warp == 8 && lane == 0) {
+    ptx::prefetch_tmap(&tmQ);
+    ptx::prefetch_tmap(&tmK);
+    ptx::prefetch_tmap(&tmV);
+    ptx::prefetch_tmap(&tmdO);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = tmem_base_slot;
+  volatile int* abort_ptr = &abort_flag;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_once = ptx::policy_evict_first();
+      const uint64_t pol_shared = ptx::policy_evict_last();
+      const uint32_t kv_full = ptx::smem_u32(&bar_kv_full);
+      ptx::mbar_arrive_expect_tx(kv_full, C::kPairBytes);
+      for (int c = 0; c < C::kChunks; ++c) {
+        ptx::tma_load_3d(sK + c * C::kChunkBytes, &tmK, kv_full, c * 64, kv0, bh, pol_once);
+        ptx::tma_load_3d(sV + c * C::kChunkBytes, &tmV, kv_full, c * 64, kv0, bh, pol_once);
+      }
+      int issued = 0;
+      bool ok = true;
+      for (int i = 0; i < n; ++i) {
+        const int slot = i % C::kStages;
+        if (!wait_or_abort(ptx::smem_u32(&bar_in_empty[slot]), ((i / C::kStages) & 1) ^ 1u, abort_ptr,
+                           p.timeout_ns, kRoleDkvProducer)) {
+          ok = false;
+          break;
+        }
+        issued = i + 1;
+        const uint32_t full = ptx::smem_u32(&bar_in_full[slot]);
+        const uint32_t dst = sRing + slot * C::kPairBytes;
+        ptx::mbar_arrive_expect_tx(full, C::kPairBytes + C::kVecBytes);
+        for (int c = 0; c < C::kChunks; ++c) {
+          ptx::tma_load_3d(dst + c * C::kChunkBytes, &tmQ, full, c * 64, i * C::kBlk, bh, pol_shared);
+          ptx::tma_load_3d(dst + C::kTileBytes + c * C::kChunkBytes, &tmdO, full, c * 64, i * C::kBlk, bh,
+                           pol_shared);
+        }
+        const size_t voff = static_cast<size_t>(bh) * p.Npad + static_cast<size_t>(i) * C::kBlk;
+        ptx::bulk_load_1d(sVec + slot * C::kVecBytes, p.nlse2 + voff, C::kBlk * 4, full, pol_shared);
+        ptx::bulk_load_1d(sVec + slot * C::kVecBytes + C::kBlk * 4, p.ndelta + voff, C::kBlk * 4, full,
+                          pol_shared);
+      }
+      if (!ok || *abort_ptr) {
+        drain_wait(kv_full, 0, p.timeout_ns);
+        for (int i = issued > C::kStages ? issued - C::kStages : 0; i < issued; ++i)
+          drain_wait(ptx::smem_u32(&bar_in_full[i % C::kStages]), (i / C::kStages) & 1, p.timeout_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      auto region = [&](int i) { return tmem_base + kColR + 128u * static_cast<uint32_t>(i & 1); };
+      auto q_tile = [&](int i) { return sRing + (i % C::kStages) * C::kPairBytes; };
+      bool ok = wait_or_abort(ptx::smem_u32(&bar_kv_full), 0, abort_ptr, p.timeout_ns, kRoleDkvMma);
+      if (ok) ok = wait_or_abort(ptx::smem_u32(&bar_in_full[0]), 0, abort_ptr, p.timeout_ns, kRoleDkvMma);
+      if (ok) {
+        ptx::tc_fence_after();
+        issue_tile_qk<HD>(region(0), sK, q_tile(0));                   // S_0^T = K Q_0^T
+        issue_tile_qk<HD>(region(1), sV, q_tile(0) + C::kTileBytes);   // dP_0^T = V dO_0^T
+        ptx::mma_commit(ptx::smem_u32(&bar_s_full));
+      }
+      for (int i = 0; i < n && ok; ++i) {
+        if (i + 1 < n) {
+          const int s1 = (i + 1) % C::kStages;
+          ok = wait_or_abort(ptx::smem_u32(&bar_in_full[s1]), ((i + 1) / C::kStages) & 1, abort_ptr, p.timeout_ns,
+                             kRoleDkvMma);
+          if (!ok) break;
+          ok = wait_or_abort(ptx::smem_u32(&bar_dp_free), i & 1, abort_ptr, p.timeout_ns, kRoleDkvMma);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          issue_tile_qk<HD>(region(i + 1), sK, q_tile(i + 1));          // S_{i+1}^T
+        }
+        ok = wait_or_abort(ptx::smem_u32(&bar_p_full), i & 1, abort_ptr, p.timeout_ns, kRoleDkvMma);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        issue_tile_acc<HD>(tmem_base + kColDV, region(i), q_tile(i) + C::kTileBytes, i > 0);   // dV += P^T dO_i
+        issue_tile_acc<HD>(tmem_base + kColDK, region(i) + 32, q_tile(i), i > 0);             // dK += dS^T Q_i
+        ptx::mma_commit(ptx::smem_u32(&bar_in_empty[i % C::kStages]));
+        if (i + 1 < n) {
+          issue_tile_qk<HD>(region(i), sV, q_tile(i + 1) + C::kTileBytes);   // dP_{i+1}^T
+          ptx::mma_commit(ptx::smem_u32(&bar_s_full));
+        }
+      }
+      if (ok) {
+        ptx::mma_commit(ptx::smem_u32(&bar_acc_full));
+      } else {
+        ptx::mma_commit(ptx::smem_u32(&bar_drain));
+        drain_wait(ptx::smem_u32(&bar_drain), 0, p.timeout_ns);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ P, dS + epilogue
+    const int quarter = warp & 3;
+    const int half = warp >> 2;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint64_t sl2x2 = ptx::f2_pack(p.scale_log2, p.scale_log2);
+    bool ok = true;
+    for (int i = 0; i < n; ++i) {
+      ok = wait_warp_or_abort(ptx::smem_u32(&bar_s_full), i & 1, abort_ptr, p.timeout_ns, kRoleDkvSoftmax);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const uint32_t tS = tmem_base + lane_addr + kColR + 128u * (i & 1) + 64u * half;
+      const uint32_t tP = tmem_base + lane_addr + kColR + 128u * ((i + 1) & 1) + 64u * half;
+      uint32_t s[2][32], dp[2][32];
+      ptx::tmem_ld32(tS, s[0]);
+      ptx::tmem_ld32(tS + 32, s[1]);
+      ptx::tmem_ld32(tP, dp[0]);
+      ptx::tmem_ld32(tP + 32, dp[1]);
+      ptx::tmem_ld_wait();
+      ptx::reg_fence32(s[0]);
+      ptx::reg_fence32(s[1]);
+      ptx::reg_fence32(dp[0]);
+      ptx::reg_fence32(dp[1]);
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(ptx::smem_u32(&bar_dp_free));
+
+      // -LSE*log2e and -D of this warp's 64 query columns (broadcast reads).
+      const float4* vl = reinterpret_cast<const float4*>(vec + (i % C::kStages) * (C::kVecBytes / 4) + 64 * half);
+      const float4* vd = vl + 32;    // + 128 floats
+      uint32_t pp[32], pds[32];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float4 l4 = vl[8 * c + u];
+          const float4 d4 = vd[8 * c + u];
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int e = 4 * u + 2 * h2;     // column within the 32-column piece
+            const uint64_t nl2 = h2 ? ptx::f2_pack(l4.z, l4.w) : ptx::f2_pack(l4.x, l4.y);
+            const uint64_t nd2 = h2 ? ptx::f2_pack(d4.z, d4.w) : ptx::f2_pack(d4.x, d4.y);
+            float x0, x1;
+            ptx::f2_unpack(
+                ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1])), sl2x2, nl2), x0,
+                x1);
+            const float p0 = ptx::ex2_approx(x0);
+            const float p1 = ptx::ex2_approx(x1);
+            const uint64_t t = ptx::f2_add(ptx::f2_pack(__uint_as_float(dp[c][e]), __uint_as_float(dp[c][e + 1])), nd2);
+            float d0, d1;
+            ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(p0, p1), t), d0, d1);
+            pp[16 * c + 2 * u + h2] = ptx::pack_bf16x2(p0, p1);
+            pds[16 * c + 2 * u + h2] = ptx::pack_bf16x2(d0, d1);
+          }
+        }
+      }
+      ptx::tmem_st32(tS, pp);
+      ptx::tmem_st32(tS + 32, pds);
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(ptx::smem_u32(&bar_p_full));
+    }
+    if (ok) ok = wait_warp_or_abort(ptx::smem_u32(&bar_acc_full), 0, abort_ptr, p.timeout_ns, kRoleDkvSoftmax);
+    if (ok) {
+      ptx::tc_fence_after();
+      const int kv = kv0 + row;
+      const size_t off = (static_cast<size_t>(bh) * p.N + kv) * HD + half * (HD / 2);
+#pragma unroll
+      for (int c = 0; c < HD / 64; ++c) {
+        store_row32(tmem_base + lane_addr + kColDV + half * (HD / 2) + 32 * c, 1.f, p.dV + off + 32 * c, kv < p.N);
+        store_row32(tmem_base + lane_addr + kColDK + half * (HD / 2) + 32 * c, p.scale, p.dK + off + 32 * c,
+                    kv < p.N);
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+}  // namespace fa

@@ -25,7 +25,7 @@ FA_ERR_TIMEOUT = 4
 
 #: every symbol include/fa.h declares
 EXPORTED = ("fa_fwd", "fa_get_device_status", "fa_status_string", "fa_last_cuda_error", "fa_fwd_fault_test",
-            "fa_naive_fwd", "fa_naive_workspace_bytes", "fa_naive_fwd_noalloc")
+            "fa_naive_fwd", "fa_naive_workspace_bytes", "fa_naive_fwd_noalloc", "fa_bwd", "fa_bwd_workspace_bytes")
 
 _lib = None
 
@@ -64,6 +64,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_naive_fwd.restype = i
     lib.fa_naive_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, vp]
     lib.fa_naive_fwd_noalloc.restype = i
+    lib.fa_bwd_workspace_bytes.argtypes = [i, i, i]
+    lib.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, vp, ctypes.c_size_t, vp]
+    lib.fa_bwd.restype = i
     _lib = lib
     return lib
 
@@ -159,6 +163,52 @@ def fa_naive_fwd(q, k, v, o=None, lse=None, scale: float | None = None, workspac
     if st != FA_OK:
         raise FaError(st, "fa_naive_fwd")
     return o, lse
+
+
+def fa_bwd_workspace_bytes(B: int, H: int, N: int) -> int:
+    return int(load_library().fa_bwd_workspace_bytes(int(B), int(H), int(N)))
+
+
+def fa_bwd(q, k, v, o, do, lse, dq=None, dk=None, dv=None, scale: float | None = None, workspace=None,
+           stream=None):
+    """Gradients (dq, dk, dv) of <do, o> for o = softmax(scale * q k^T) v, with
+    the probabilities rebuilt from the forward's ``lse`` and ``o``.
+
+    q, k, v, o, do: bf16 CUDA tensors [B, H, N, d], contiguous; lse: float32
+    [B, H, N]. Outputs (bf16, shaped like q) and the workspace (at least
+    fa_bwd_workspace_bytes(B, H, N) bytes) are allocated with torch when not
+    given. ``scale`` defaults to 1/sqrt(d). Returns (dq, dk, dv).
+    """
+    _check_qkv(q, k, v)
+    B, H, N, d = q.shape
+    for name, t in (("o", o), ("do", do)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or t.shape != q.shape \
+                or not t.is_contiguous() or t.device != q.device:
+            raise ValueError(f"{name} must be a contiguous bf16 tensor shaped like q on q's device")
+    if not isinstance(lse, torch.Tensor) or lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) \
+            or not lse.is_contiguous() or lse.device != q.device:
+        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor on q's device")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    outs = []
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        if t is None:
+            t = torch.empty_like(q)
+        elif t.dtype != torch.bfloat16 or t.shape != q.shape or not t.is_contiguous() or t.device != q.device:
+            raise ValueError(f"{name} must be a contiguous bf16 tensor shaped like q on q's device")
+        outs.append(t)
+    need = fa_bwd_workspace_bytes(B, H, N)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                        outs[0].data_ptr(), outs[1].data_ptr(), outs[2].data_ptr(), B, H, N, d, float(scale),
+                        workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                        _stream_handle(stream, q.device))
+    if st != FA_OK:
+        raise FaError(st, "fa_bwd")
+    return tuple(outs)
 
 
 def fa_fwd_fault_test(q, k, v, o, lse, scale: float, drop_load: int, timeout_ns: int, stream=None) -> int:

@@ -5,6 +5,8 @@ the one module that both the oracle side (tests, CPU baseline) and the CUDA
 side (tests, bench) use, so that both see the identical bf16 bits.
 
 Recipe (the pages name no dataset; every input is synthetic):
+  * the backward pass's incoming gradient dO: standard normal, bf16, from a
+    generator of its own (``make_grad``);
   * a ``torch.Generator`` on the CPU, seeded with ``seed``;
   * Q, K, V drawn in that order in float32 with the distribution the workload
     names, then rounded to bf16 (round-to-nearest-even, torch's conversion);
@@ -25,7 +27,7 @@ from dataclasses import dataclass
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "workload", "make_inputs", "make_random", "sha256_of"]
+__all__ = ["Workload", "WORKLOADS", "workload", "make_inputs", "make_random", "make_grad", "sha256_of"]
 
 
 @dataclass(frozen=True)
@@ -115,6 +117,15 @@ def make_inputs(w: Workload):
     q, k, v = make_random(w.B, w.H, w.N, w.d, w.seed, w.q_dist, w.k_dist, w.v_dist,
                           w.spike_frac, w.spike_mult)
     return q, k, v, w.scale
+
+
+def make_grad(B: int, H: int, N: int, d: int, seed: int) -> torch.Tensor:
+    """The incoming gradient dO of the backward pass: bf16 [B, H, N, d], standard
+    normal, drawn on the CPU from its own generator seeded with ``seed + 7919``
+    (so that it never repeats the Q, K, V stream of the same seed)."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(int(seed) + 7919)
+    return _draw(gen, (B, H, N, d), "normal")
 
 
 def sha256_of(*tensors: torch.Tensor) -> str:

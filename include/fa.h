@@ -1,5 +1,6 @@
 /*
- * fa.h -- C ABI of the exact attention forward pass for GB300 (sm_103a).
+ * fa.h -- C ABI of the exact attention forward pass (and its backward by
+ * recomputation) for GB300 (sm_103a).
  *
  * The operation: for every batch b and head h,
  *     S = scale * Q K^T              (N x N scores, never written to memory)
@@ -78,7 +79,8 @@ fa_status_t fa_fwd(const void* Q, const void* K, const void* V, void* O, float* 
  * FA_ERR_TIMEOUT if any kernel of this library on this device gave up on a
  * wait since the last call, or FA_ERR_CUDA if the synchronisation failed.
  * `info`, if not NULL, receives 4 words describing the first timeout:
- * {role (1 producer, 2 mma, 3 softmax/epilogue), blockIdx.x, blockIdx.y,
+ * {role (forward: 1 producer, 2 mma, 3 softmax/epilogue; backward dQ kernel:
+ * 4, 5, 6; backward dK/dV kernel: 7, 8, 9, in the same order), blockIdx.x, blockIdx.y,
  * blockIdx.z}; all zero when there was none.
  */
 fa_status_t fa_get_device_status(cudaStream_t stream, unsigned int* info);
@@ -137,6 +139,42 @@ fa_status_t fa_naive_fwd(const void* Q, const void* K, const void* V, void* O, f
  */
 fa_status_t fa_naive_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE,
                                  int B, int H, int N, int d, float scale, cudaStream_t stream);
+
+/*
+ * fa_bwd_workspace_bytes -- bytes of device workspace fa_bwd needs for
+ * B x H heads of length N: two float32 values per query row, rows padded to
+ * a multiple of 128. Returns 0 for non-positive sizes.
+ */
+size_t fa_bwd_workspace_bytes(int B, int H, int N);
+
+/*
+ * fa_bwd -- exact attention backward pass by recomputation. For every (b, h)
+ * it forms the gradients of <dO, O> for O = softmax(scale Q K^T) V:
+ *     P  = exp(scale Q K^T - LSE)   (rebuilt from the forward's LSE)
+ *     D  = rowsum(dO * O)           (from the forward's O)
+ *     dV = P^T dO,   dS = P * (dO V^T - D),   dQ = scale dS K,   dK = scale dS^T Q
+ * without writing any N x N matrix to memory ("01 · 注意力为什么是 IO 瓶颈"
+ * §7: only O and LSE are kept from the forward and P is recomputed instead
+ * of being stored and read back; the gradient formulas are the chain rule of
+ * the forward's definition, which the pages do not print).
+ *   Q, K, V, O, dO : device, bf16 [B, H, N, d], read only. O and LSE are the
+ *                    outputs of fa_fwd (or any forward with the same meaning).
+ *   LSE            : device, float32 [B, H, N], read only, natural log.
+ *   dQ, dK, dV     : device, bf16 [B, H, N, d], written (every element).
+ *   workspace      : device, at least fa_bwd_workspace_bytes(B, H, N) bytes,
+ *                    128-byte aligned, owned by the caller; overwritten.
+ *   B, H, N, d, scale, stream : as for fa_fwd (same limits).
+ * Three kernel launches on `stream`: a per-row pass over O and dO, then the
+ * dQ kernel (one CTA per 128 query rows) and the dK/dV kernel (one CTA per
+ * 128 key rows). Inputs must be 16-byte aligned (LSE 4-byte); dQ, dK, dV and
+ * the workspace must not overlap any input or each other. Errors as for
+ * fa_fwd, plus FA_ERR_INVALID_ARG for a missing, misaligned, too small or
+ * overlapping output or workspace.
+ */
+fa_status_t fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                   const float* LSE, void* dQ, void* dK, void* dV,
+                   int B, int H, int N, int d, float scale,
+                   void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * fa_fwd_fault_test -- TEST HOOK, not for production use. Same as fa_fwd,

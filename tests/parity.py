@@ -104,3 +104,70 @@ def check_sampled(q, k, v, scale, n_rows=256, seed=0, two_x_rule=True):
     slack = 1e-2 * (vmax - vmin) + 1e-6
     assert bool((of >= vmin - slack).all()) and bool((of <= vmax + slack).all())
     return err
+
+
+# --- backward ------------------------------------------------------------------
+# Tolerances for dQ, dK, dV (bf16 outputs), against the float64 backward oracle
+# on the identical bf16 inputs and the oracle's forward O (rounded to bf16, as
+# a forward pass hands it over) and LSE (float32):
+#   max |err| <= 2 x the max |err| of the bf16 materialise-path backward
+#               (the same "twice the baseline" rule as the forward, §7)
+#   ||err||_F <= 1e-2 ||ref||_F + 1e-6 sqrt(size)   (bf16 output rounding is
+#               2^-9 relative; the floor covers an all-zero reference, N = 1)
+TOL_BWD_FRO = 1e-2
+
+
+def oracle_forward_inputs(q, k, v, scale):
+    """O (bf16) and LSE (float32) from the float64 forward oracle: the
+    backward's O/LSE inputs come from the oracle, never from the CUDA path."""
+    O, L = oracle.attention(to64(q), to64(k), to64(v), scale)
+    return torch.from_numpy(O).to(torch.bfloat16), torch.from_numpy(L).to(torch.float32)
+
+
+def run_gpu_bwd(q, k, v, o, do, lse, scale, device="cuda:0", stream=None):
+    from exact_io_aware_34_gb300 import fa
+    args = [x.to(device) for x in (q, k, v, o, do, lse)]
+    dq, dk, dv = fa.fa_bwd(*args, scale=scale, stream=stream)
+    torch.cuda.synchronize(device)
+    st, info = fa.fa_get_device_status()
+    assert st == fa.FA_OK, (fa.fa_status_string(st), info)
+    return dq.cpu(), dk.cpu(), dv.cpu()
+
+
+def bwd_errors(got, ref, naive=None):
+    """Per-gradient error figures; ``got`` bf16 tensors, ``ref``/``naive`` float64."""
+    out = {}
+    for name, g, r, nv in zip(("dq", "dk", "dv"), got, ref, naive if naive is not None else (None,) * 3):
+        g64 = to64(g) if isinstance(g, torch.Tensor) else g
+        e = g64 - r
+        out[name] = {
+            "max": float(np.abs(e).max()),
+            "fro": float(np.linalg.norm(e)),
+            "ref_fro": float(np.linalg.norm(r)),
+            "ref_max": float(np.abs(r).max()),
+            "size": int(r.size),
+            "finite": bool(np.isfinite(g64).all()),
+        }
+        if nv is not None:
+            out[name]["naive_max"] = float(np.abs(nv - r).max())
+    return out
+
+
+def assert_bwd_within(err, two_x_rule=True):
+    for name, e in err.items():
+        assert e["finite"], (name, e)
+        assert e["fro"] <= TOL_BWD_FRO * e["ref_fro"] + 1e-6 * np.sqrt(e["size"]), (name, e)
+        if two_x_rule and "naive_max" in e:
+            assert e["max"] <= 2 * e["naive_max"], (name, e)
+
+
+def check_bwd_full(q, k, v, do, scale, two_x_rule=True):
+    """Whole-gradient parity (sizes the oracle evaluates in seconds)."""
+    o, lse = oracle_forward_inputs(q, k, v, scale)
+    got = run_gpu_bwd(q, k, v, o, do, lse, scale)
+    Q, K, V, dO = (to64(x) for x in (q, k, v, do))
+    ref = oracle.attention_bwd(Q, K, V, dO, scale)
+    naive = oracle.naive_bf16_attention_bwd(Q, K, V, dO, scale) if two_x_rule else None
+    err = bwd_errors(got, ref, naive)
+    assert_bwd_within(err, two_x_rule)
+    return err, got

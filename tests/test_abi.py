@@ -124,3 +124,47 @@ def test_naive_workspace_size(lib):
 ])
 def test_naive_host_side_rejections(lib, kwargs, expect):
     assert naive_call(lib, **kwargs) == expect
+
+
+def bwd_call(lib, **kw):
+    args = dict(Q=A, K=A + GAP, V=A + 2 * GAP, O=A + 3 * GAP, L=A + 4 * GAP, dO=A + 5 * GAP, dQ=A + 6 * GAP,
+                dK=A + 7 * GAP, dV=A + 8 * GAP, ws=A + 9 * GAP, ws_bytes=1 << 40, B=1, H=1, N=128, d=128,
+                scale=0.1)
+    args.update(kw)
+    return lib.fa_bwd(args["Q"], args["K"], args["V"], args["O"], args["dO"], args["L"], args["dQ"], args["dK"],
+                      args["dV"], args["B"], args["H"], args["N"], args["d"], ctypes.c_float(args["scale"]),
+                      args["ws"], args["ws_bytes"], None)
+
+
+def test_bwd_workspace_size(lib):
+    assert fa.fa_bwd_workspace_bytes(1, 1, 128) == 2 * 128 * 4
+    assert fa.fa_bwd_workspace_bytes(2, 3, 100) == 2 * 6 * 128 * 4       # rows padded to 128
+    assert fa.fa_bwd_workspace_bytes(1, 2, 129) == 2 * 2 * 256 * 4
+    assert fa.fa_bwd_workspace_bytes(1, 0, 128) == 0
+
+
+@pytest.mark.parametrize("kwargs,expect", [
+    (dict(dO=0), fa.FA_ERR_INVALID_ARG),
+    (dict(dQ=0), fa.FA_ERR_INVALID_ARG),
+    (dict(dK=0), fa.FA_ERR_INVALID_ARG),
+    (dict(dV=0), fa.FA_ERR_INVALID_ARG),
+    (dict(ws=0), fa.FA_ERR_INVALID_ARG),
+    (dict(Q=0), fa.FA_ERR_INVALID_ARG),
+    (dict(L=0), fa.FA_ERR_INVALID_ARG),
+    (dict(dO=A + 5 * GAP + 8), fa.FA_ERR_INVALID_ARG),           # not 16-byte aligned
+    (dict(dK=A + 7 * GAP + 4), fa.FA_ERR_INVALID_ARG),
+    (dict(ws=A + 9 * GAP + 64), fa.FA_ERR_INVALID_ARG),          # workspace not 128-byte aligned
+    (dict(ws_bytes=2 * 128 * 4 - 1), fa.FA_ERR_INVALID_ARG),     # workspace too small
+    (dict(dQ=A + 512), fa.FA_ERR_INVALID_ARG),                   # dQ overlaps Q
+    (dict(dV=A + 5 * GAP), fa.FA_ERR_INVALID_ARG),               # dV overlaps dO
+    (dict(dK=A + 4 * GAP), fa.FA_ERR_INVALID_ARG),               # dK overlaps LSE
+    (dict(dK=A + 6 * GAP + 256), fa.FA_ERR_INVALID_ARG),         # dK overlaps dQ
+    (dict(ws=A + 8 * GAP), fa.FA_ERR_INVALID_ARG),               # workspace overlaps dV
+    (dict(ws=A + 3 * GAP), fa.FA_ERR_INVALID_ARG),               # workspace overlaps O
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(scale=-1.0), fa.FA_ERR_UNSUPPORTED),
+    (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(N=0), fa.FA_ERR_INVALID_ARG),
+])
+def test_bwd_host_side_rejections(lib, kwargs, expect):
+    assert bwd_call(lib, **kwargs) == expect
