@@ -263,7 +263,7 @@ fa_status_t bwd_launch(const void* Q, const void* K, const void* V, const void* 
   static cudaError_t attr_err[64];
   std::call_once(once[dev], [&] {
     attr_err[dev] = cudaFuncSetAttribute(fa::fa_bwd_dq_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
+                                         fa::DqCfg<HD>::kSmemBytes);
     if (attr_err[dev] == cudaSuccess)
       attr_err[dev] = cudaFuncSetAttribute(fa::fa_bwd_dkdv_kernel<HD>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
@@ -300,7 +300,7 @@ fa_status_t bwd_launch(const void* Q, const void* K, const void* V, const void* 
   if (e != cudaSuccess) return cuda_fail(e);
   const dim3 grid(static_cast<unsigned>(p.n_blocks), H, B);
   // 2. dQ, one CTA per 128 query rows
-  fa::fa_bwd_dq_kernel<HD><<<grid, C::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
+  fa::fa_bwd_dq_kernel<HD><<<grid, C::kThreads, fa::DqCfg<HD>::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   // 3. dK and dV, one CTA per 128 key rows

@@ -146,15 +146,16 @@ __device__ __forceinline__ void issue_tile_qk(uint32_t d_tmem, uint32_t a_tile, 
 }
 
 // Accumulating product over the 128 streamed rows: D[128 x HD] += A B with A
-// packed bf16 in TMEM (the layout described at the top of this file, base
-// column a_col) and B a 128 x HD tile read MN-major from shared memory.
-template <int HD>
+// packed bf16 in TMEM (rows 64h .. 64h+63 of the streamed block at column
+// a_col + kHalf * h, 16 rows per 8 columns) and B a 128 x HD tile read
+// MN-major from shared memory.
+template <int HD, int kHalf>
 __device__ __forceinline__ void issue_tile_acc(uint32_t d_tmem, uint32_t a_col, uint32_t b_tile, bool accumulate) {
   using C = BwdCfg<HD>;
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
     const uint64_t b_desc = ptx::desc_mnmajor_sw128(b_tile + kk * 16 * 128, C::kChunkBytes);
-    ptx::mma_ts(d_tmem, a_col + 64 * (kk >> 2) + 8 * (kk & 3), b_desc, C::kIdescAcc,
+    ptx::mma_ts(d_tmem, a_col + kHalf * (kk >> 2) + 8 * (kk & 3), b_desc, C::kIdescAcc,
                 (accumulate || kk > 0) ? 1u : 0u);
   }
 }
@@ -179,21 +180,41 @@ __device__ __forceinline__ void store_row32(uint32_t taddr, float mul, __nv_bflo
 }
 
 // ---------------------------------------------------------------- dQ
+// Shared memory: Q and dO of the CTA's query block, a ring of kKSlots K tiles
+// and one of kVSlots V tiles (K_j is read twice, by S_j early and by dQ_j
+// late; V_j only by dP_j). TMEM: dQ at 0, S at HD, dP at HD + 128, and two
+// 64-column slots for the packed dS of consecutive blocks at HD + 256. With
+// dS outside the score regions, S_{j+1} and dP_{j+1} are issued as soon as
+// the elementwise warps have loaded S_j and dP_j, and the elementwise step of
+// block j+1 overlaps dQ += dS_j K_j.
+template <int HD>
+struct DqCfg {
+  using C = BwdCfg<HD>;
+  static constexpr int kKSlots = (HD == 128) ? 3 : 4;
+  static constexpr int kVSlots = (HD == 128) ? 2 : 4;
+  static constexpr int kSmemBytes = (2 + kKSlots + kVSlots) * C::kTileBytes + 1024;
+  static constexpr uint32_t kColDQ = 0;
+  static constexpr uint32_t kColS = HD;
+  static constexpr uint32_t kColP = HD + 128;
+  static constexpr uint32_t kColDS = HD + 256;    // + 64 * (j & 1)
+};
+
 template <int HD>
 __global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                      const BwdParams p) {
   using C = BwdCfg<HD>;
-  constexpr uint32_t kColDQ = 0;
-  constexpr uint32_t kColR = HD;    // R0 = kColR, R1 = kColR + 128
+  using D = DqCfg<HD>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_in_full;
-  __shared__ __align__(8) uint64_t bar_kv_full[C::kStages];
-  __shared__ __align__(8) uint64_t bar_kv_empty[C::kStages];
+  __shared__ __align__(8) uint64_t bar_k_full[D::kKSlots];
+  __shared__ __align__(8) uint64_t bar_k_empty[D::kKSlots];
+  __shared__ __align__(8) uint64_t bar_v_full[D::kVSlots];
+  __shared__ __align__(8) uint64_t bar_v_empty[D::kVSlots];
   __shared__ __align__(8) uint64_t bar_s_full;
   __shared__ __align__(8) uint64_t bar_dp_free;
-  __shared__ __align__(8) uint64_t bar_p_full;
+  __shared__ __align__(8) uint64_t bar_p_full[2];
   __shared__ __align__(8) uint64_t bar_acc_full;
   __shared__ __align__(8) uint64_t bar_drain;
   __shared__ uint32_t tmem_base_slot;
@@ -208,17 +229,23 @@ __global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
   const uint32_t smem_base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t sQ = smem_base;
   const uint32_t sdO = smem_base + C::kTileBytes;
-  const uint32_t sRing = smem_base + C::kPairBytes;    // slot s: K_j at s * pair, V_j at s * pair + tile
+  const uint32_t sK = smem_base + 2 * C::kTileBytes;                    // kKSlots tiles
+  const uint32_t sV = sK + D::kKSlots * C::kTileBytes;                  // kVSlots tiles
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(ptx::smem_u32(&bar_in_full), 1);
-    for (int s = 0; s < C::kStages; ++s) {
-      ptx::mbar_init(ptx::smem_u32(&bar_kv_full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bar_kv_empty[s]), 1);
+    for (int s = 0; s < D::kKSlots; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&bar_k_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bar_k_empty[s]), 1);
+    }
+    for (int s = 0; s < D::kVSlots; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&bar_v_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bar_v_empty[s]), 1);
     }
     ptx::mbar_init(ptx::smem_u32(&bar_s_full), 1);
     ptx::mbar_init(ptx::smem_u32(&bar_dp_free), 256);
-    ptx::mbar_init(ptx::smem_u32(&bar_p_full), 256);
+    ptx::mbar_init(ptx::smem_u32(&bar_p_full[0]), 256);
+    ptx::mbar_init(ptx::smem_u32(&bar_p_full[1]), 256);
     ptx::mbar_init(ptx::smem_u32(&bar_acc_full), 1);
     ptx::mbar_init(ptx::smem_u32(&bar_drain), 1);
     abort_flag = 0;
@@ -246,70 +273,81 @@ __global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
       const uint64_t pol_once = ptx::policy_evict_first();
       const uint64_t pol_shared = ptx::policy_evict_last();
       const uint32_t in_full = ptx::smem_u32(&bar_in_full);
-      ptx::mbar_arrive_expect_tx(in_full, C::kPairBytes);
+      ptx::mbar_arrive_expect_tx(in_full, 2 * C::kTileBytes);
       for (int c = 0; c < C::kChunks; ++c) {
         ptx::tma_load_3d(sQ + c * C::kChunkBytes, &tmQ, in_full, c * 64, q0, bh, pol_once);
         ptx::tma_load_3d(sdO + c * C::kChunkBytes, &tmdO, in_full, c * 64, q0, bh, pol_once);
       }
-      int issued = 0;
+      // Loads in the order they are needed: K_0, V_0, K_1, V_1, ...
+      int issued = 0;    // loads started, counted in that order
       bool ok = true;
-      for (int j = 0; j < n; ++j) {
-        const int slot = j % C::kStages;
-        if (!wait_or_abort(ptx::smem_u32(&bar_kv_empty[slot]), ((j / C::kStages) & 1) ^ 1u, abort_ptr,
-                           p.timeout_ns, kRoleDqProducer)) {
+      for (int it = 0; it < 2 * n && ok; ++it) {
+        const int j = it >> 1;
+        const bool is_v = it & 1;
+        const int slots = is_v ? D::kVSlots : D::kKSlots;
+        const int slot = j % slots;
+        uint64_t* empty = is_v ? bar_v_empty : bar_k_empty;
+        uint64_t* full = is_v ? bar_v_full : bar_k_full;
+        if (!wait_or_abort(ptx::smem_u32(&empty[slot]), ((j / slots) & 1) ^ 1u, abort_ptr, p.timeout_ns,
+                           kRoleDqProducer)) {
           ok = false;
           break;
         }
-        issued = j + 1;
-        const uint32_t full = ptx::smem_u32(&bar_kv_full[slot]);
-        const uint32_t dst = sRing + slot * C::kPairBytes;
-        ptx::mbar_arrive_expect_tx(full, C::kPairBytes);
-        for (int c = 0; c < C::kChunks; ++c) {
-          ptx::tma_load_3d(dst + c * C::kChunkBytes, &tmK, full, c * 64, j * C::kBlk, bh, pol_shared);
-          ptx::tma_load_3d(dst + C::kTileBytes + c * C::kChunkBytes, &tmV, full, c * 64, j * C::kBlk, bh,
-                           pol_shared);
-        }
+        issued = it + 1;
+        const uint32_t fb = ptx::smem_u32(&full[slot]);
+        ptx::mbar_arrive_expect_tx(fb, C::kTileBytes);
+        const uint32_t dst = (is_v ? sV : sK) + slot * C::kTileBytes;
+        for (int c = 0; c < C::kChunks; ++c)
+          ptx::tma_load_3d(dst + c * C::kChunkBytes, is_v ? &tmV : &tmK, fb, c * 64, j * C::kBlk, bh, pol_shared);
       }
       if (!ok || *abort_ptr) {
         drain_wait(in_full, 0, p.timeout_ns);
-        for (int j = issued > C::kStages ? issued - C::kStages : 0; j < issued; ++j)
-          drain_wait(ptx::smem_u32(&bar_kv_full[j % C::kStages]), (j / C::kStages) & 1, p.timeout_ns);
+        // Only the last kKSlots K loads and kVSlots V loads can still be in flight.
+        for (int it = 0; it < issued; ++it) {
+          const int j = it >> 1;
+          const bool is_v = it & 1;
+          const int slots = is_v ? D::kVSlots : D::kKSlots;
+          const int last_j = ((issued - 1 - (is_v ? 1 : 0)) >> 1);
+          if (j + slots <= last_j) continue;
+          drain_wait(ptx::smem_u32(&(is_v ? bar_v_full : bar_k_full)[j % slots]), (j / slots) & 1, p.timeout_ns);
+        }
       }
     }
     __syncwarp();
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      auto region = [&](int j) { return tmem_base + kColR + 128u * static_cast<uint32_t>(j & 1); };
-      auto k_tile = [&](int j) { return sRing + (j % C::kStages) * C::kPairBytes; };
-      bool ok = wait_or_abort(ptx::smem_u32(&bar_in_full), 0, abort_ptr, p.timeout_ns, kRoleDqMma);
-      if (ok) ok = wait_or_abort(ptx::smem_u32(&bar_kv_full[0]), 0, abort_ptr, p.timeout_ns, kRoleDqMma);
-      if (ok) {
+      auto k_tile = [&](int j) { return sK + (j % D::kKSlots) * C::kTileBytes; };
+      auto v_tile = [&](int j) { return sV + (j % D::kVSlots) * C::kTileBytes; };
+      // S_j = Q K_j^T and dP_j = dO V_j^T, after K_j and V_j have landed.
+      auto issue_sdp = [&](int j) -> bool {
+        if (!wait_or_abort(ptx::smem_u32(&bar_k_full[j % D::kKSlots]), (j / D::kKSlots) & 1, abort_ptr,
+                           p.timeout_ns, kRoleDqMma))
+          return false;
+        if (!wait_or_abort(ptx::smem_u32(&bar_v_full[j % D::kVSlots]), (j / D::kVSlots) & 1, abort_ptr,
+                           p.timeout_ns, kRoleDqMma))
+          return false;
         ptx::tc_fence_after();
-        issue_tile_qk<HD>(region(0), sQ, k_tile(0));                   // S_0 = Q K_0^T
-        issue_tile_qk<HD>(region(1), sdO, k_tile(0) + C::kTileBytes);  // dP_0 = dO V_0^T
+        issue_tile_qk<HD>(tmem_base + D::kColS, sQ, k_tile(j));
+        issue_tile_qk<HD>(tmem_base + D::kColP, sdO, v_tile(j));
+        ptx::mma_commit(ptx::smem_u32(&bar_v_empty[j % D::kVSlots]));
         ptx::mma_commit(ptx::smem_u32(&bar_s_full));
-      }
+        return true;
+      };
+      bool ok = wait_or_abort(ptx::smem_u32(&bar_in_full), 0, abort_ptr, p.timeout_ns, kRoleDqMma);
+      if (ok) ok = issue_sdp(0);
       for (int j = 0; j < n && ok; ++j) {
         if (j + 1 < n) {
-          const int s1 = (j + 1) % C::kStages;
-          ok = wait_or_abort(ptx::smem_u32(&bar_kv_full[s1]), ((j + 1) / C::kStages) & 1, abort_ptr, p.timeout_ns,
-                             kRoleDqMma);
-          if (!ok) break;
           ok = wait_or_abort(ptx::smem_u32(&bar_dp_free), j & 1, abort_ptr, p.timeout_ns, kRoleDqMma);
           if (!ok) break;
-          ptx::tc_fence_after();
-          issue_tile_qk<HD>(region(j + 1), sQ, k_tile(j + 1));          // S_{j+1}
+          ok = issue_sdp(j + 1);
+          if (!ok) break;
         }
-        ok = wait_or_abort(ptx::smem_u32(&bar_p_full), j & 1, abort_ptr, p.timeout_ns, kRoleDqMma);
+        ok = wait_or_abort(ptx::smem_u32(&bar_p_full[j & 1]), (j >> 1) & 1, abort_ptr, p.timeout_ns, kRoleDqMma);
         if (!ok) break;
         ptx::tc_fence_after();
-        issue_tile_acc<HD>(tmem_base + kColDQ, region(j), k_tile(j), j > 0);   // dQ += dS_j K_j
-        ptx::mma_commit(ptx::smem_u32(&bar_kv_empty[j % C::kStages]));
-        if (j + 1 < n) {
-          issue_tile_qk<HD>(region(j), sdO, k_tile(j + 1) + C::kTileBytes);   // dP_{j+1}
-          ptx::mma_commit(ptx::smem_u32(&bar_s_full));
-        }
+        issue_tile_acc<HD, 32>(tmem_base + D::kColDQ, tmem_base + D::kColDS + 64u * (j & 1), k_tile(j), j > 0);
+        ptx::mma_commit(ptx::smem_u32(&bar_k_empty[j % D::kKSlots]));
       }
       if (ok) {
         ptx::mma_commit(ptx::smem_u32(&bar_acc_full));
@@ -331,13 +369,13 @@ __global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
     const uint64_t sl2x2 = ptx::f2_pack(p.scale_log2, p.scale_log2);
     const uint64_t nlx2 = ptx::f2_pack(nl, nl);
     const uint64_t ndx2 = ptx::f2_pack(nd, nd);
+    const uint32_t tS = tmem_base + lane_addr + D::kColS + 64u * half;
+    const uint32_t tP = tmem_base + lane_addr + D::kColP + 64u * half;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       ok = wait_warp_or_abort(ptx::smem_u32(&bar_s_full), j & 1, abort_ptr, p.timeout_ns, kRoleDqSoftmax);
       if (!ok) break;
       ptx::tc_fence_after();
-      const uint32_t tS = tmem_base + lane_addr + kColR + 128u * (j & 1) + 64u * half;
-      const uint32_t tP = tmem_base + lane_addr + kColR + 128u * ((j + 1) & 1) + 64u * half;
       uint32_t s[2][32], dp[2][32];
       ptx::tmem_ld32(tS, s[0]);
       ptx::tmem_ld32(tS + 32, s[1]);
@@ -375,10 +413,10 @@ __global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
           pds[16 * c + k] = ptx::pack_bf16x2(d0, d1);
         }
       }
-      ptx::tmem_st32(tS, pds);
+      ptx::tmem_st32(tmem_base + lane_addr + D::kColDS + 64u * (j & 1) + 32u * half, pds);
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(ptx::smem_u32(&bar_p_full));
+      ptx::mbar_arrive(ptx::smem_u32(&bar_p_full[j & 1]));
     }
     if (ok) ok = wait_warp_or_abort(ptx::smem_u32(&bar_acc_full), 0, abort_ptr, p.timeout_ns, kRoleDqSoftmax);
     if (ok) {
@@ -387,7 +425,7 @@ __global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
       __nv_bfloat16* dst = p.dQ + (static_cast<size_t>(bh) * p.N + q) * HD + half * (HD / 2);
 #pragma unroll
       for (int c = 0; c < HD / 64; ++c)
-        store_row32(tmem_base + lane_addr + kColDQ + half * (HD / 2) + 32 * c, p.scale, dst + 32 * c, q < p.N);
+        store_row32(tmem_base + lane_addr + D::kColDQ + half * (HD / 2) + 32 * c, p.scale, dst + 32 * c, q < p.N);
     }
   }
 
@@ -533,8 +571,8 @@ __global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
         ok = wait_or_abort(ptx::smem_u32(&bar_p_full), i & 1, abort_ptr, p.timeout_ns, kRoleDkvMma);
         if (!ok) break;
         ptx::tc_fence_after();
-        issue_tile_acc<HD>(tmem_base + kColDV, region(i), q_tile(i) + C::kTileBytes, i > 0);   // dV += P^T dO_i
-        issue_tile_acc<HD>(tmem_base + kColDK, region(i) + 32, q_tile(i), i > 0);             // dK += dS^T Q_i
+        issue_tile_acc<HD, 64>(tmem_base + kColDV, region(i), q_tile(i) + C::kTileBytes, i > 0);   // dV += P^T dO_i
+        issue_tile_acc<HD, 64>(tmem_base + kColDK, region(i) + 32, q_tile(i), i > 0);             // dK += dS^T Q_i
         ptx::mma_commit(ptx::smem_u32(&bar_in_empty[i % C::kStages]));
         if (i + 1 < n) {
           issue_tile_qk<HD>(region(i), sV, q_tile(i + 1) + C::kTileBytes);   // dP_{i+1}^T
