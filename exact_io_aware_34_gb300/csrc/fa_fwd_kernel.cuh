@@ -281,22 +281,19 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
                       C::kIdescQK, kk > 0 ? 1u : 0u);
         }
       };
+      // K_0 is waited for here; every later K_{j+1} and V_j is waited for by
+      // the softmax warps before their hand-off for block j (p_full), so the
+      // p_full waits below imply those tiles have landed. An mbarrier wait in
+      // this thread stalls the queued tensor-core work, so it does as few as
+      // it can.
+      if (ok) ok = wait_or_abort(ptx::smem_u32(&bar_kv_full[0]), 0, abort_ptr, p.timeout_ns, kRoleMma);
       for (int j = 0; j < n_kv && ok; ++j) {
         const int itK = 2 * j;
-        ok = wait_or_abort(ptx::smem_u32(&bar_kv_full[itK % C::kStages]), (itK / C::kStages) & 1, abort_ptr,
-                           p.timeout_ns, kRoleMma);
-        if (!ok) break;
         ptx::tc_fence_after();
         for (int t = 0; t < 2 && ok; ++t) {
           if (j > 0) {
             ok = wait_or_abort(ptx::smem_u32(&bar_p_full[t]), (j - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
             if (!ok) break;
-            if (t == 0) {
-              const int itV = 2 * (j - 1) + 1;
-              ok = wait_or_abort(ptx::smem_u32(&bar_kv_full[itV % C::kStages]), (itV / C::kStages) & 1,
-                                 abort_ptr, p.timeout_ns, kRoleMma);
-              if (!ok) break;
-            }
             ptx::tc_fence_after();
             issue_pv(t, j - 1);
             if (t == 1) ptx::mma_commit(ptx::smem_u32(&bar_kv_empty[(2 * (j - 1) + 1) % C::kStages]));
@@ -310,12 +307,6 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
       for (int t = 0; t < 2 && ok; ++t) {
         ok = wait_or_abort(ptx::smem_u32(&bar_p_full[t]), (n_kv - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
         if (!ok) break;
-        if (t == 0) {
-          const int itV = 2 * (n_kv - 1) + 1;
-          ok = wait_or_abort(ptx::smem_u32(&bar_kv_full[itV % C::kStages]), (itV / C::kStages) & 1, abort_ptr,
-                             p.timeout_ns, kRoleMma);
-          if (!ok) break;
-        }
         ptx::tc_fence_after();
         issue_pv(t, n_kv - 1);
         ptx::mma_commit(ptx::smem_u32(&bar_o_full[t]));
@@ -341,6 +332,17 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
     float l = 0.f;          // running sum of exp, relative to m_use
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
+      // V_j and K_{j+1} must have landed before this block's hand-off (see
+      // the MMA issuer); waiting here costs nothing, S_t(j) comes later.
+      {
+        const int itV = 2 * j + 1;
+        ok = wait_warp_or_abort(ptx::smem_u32(&bar_kv_full[itV % C::kStages]), (itV / C::kStages) & 1, abort_ptr,
+                                p.timeout_ns, kRoleSoftmax);
+        if (ok && j + 1 < n_kv)
+          ok = wait_warp_or_abort(ptx::smem_u32(&bar_kv_full[(itV + 1) % C::kStages]), ((itV + 1) / C::kStages) & 1,
+                                  abort_ptr, p.timeout_ns, kRoleSoftmax);
+        if (!ok) break;
+      }
       ok = wait_warp_or_abort(ptx::smem_u32(&bar_s_full[t]), j & 1, abort_ptr, p.timeout_ns, kRoleSoftmax);
       if (!ok) break;
       ptx::tc_fence_after();
