@@ -40,16 +40,19 @@ METRIC = "attention fwd TFLOP/s (4·B·H·N²·d) and % of GB300 dense BF16 peak
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "prefill8k_d128_h32"
 KERNEL_NAME = "fa_fwd_kernel<128>"
-KERNEL_SOURCES = ["exact_io_aware_34_gb300/csrc/fa_api.cu", "exact_io_aware_34_gb300/csrc/fa_fwd_kernel.cuh",
-                  "exact_io_aware_34_gb300/csrc/sm103a_ptx.cuh"]
+# Sources that determine each kernel's machine code: a committed DRAM-traffic
+# figure is used only while these are unchanged since its capture.
+KERNEL_SOURCES = ["exact_io_aware_34_gb300/csrc/fa_fwd_kernel.cuh", "exact_io_aware_34_gb300/csrc/sm103a_ptx.cuh"]
+BWD_KERNEL_SOURCES = ["exact_io_aware_34_gb300/csrc/fa_bwd_kernel.cuh", "exact_io_aware_34_gb300/csrc/fa_fwd_kernel.cuh",
+                      "exact_io_aware_34_gb300/csrc/sm103a_ptx.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 
 
 # ----------------------------------------------------------------------------- helpers
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in (KERNEL_SOURCES if sources is None else sources):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -65,16 +68,16 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def load_traffic(workload: str):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
-    current kernel sources; otherwise None."""
+def load_traffic(workload: str, key_suffix: str = "", sources=None):
+    """DRAM bytes per launch (per call for the backward) from a committed ncu
+    summary, if it was taken on the current kernel sources; otherwise None."""
     try:
         with open(TRAFFIC_FILE) as f:
             t = json.load(f)
     except (OSError, ValueError):
         return None
-    entry = t.get(workload)
-    if not entry or entry.get("kernel_source_hash") != kernel_source_hash():
+    entry = t.get(workload + key_suffix)
+    if not entry or entry.get("kernel_source_hash") != kernel_source_hash(sources):
         return None
     return entry.get("dram_bytes_per_launch")
 
@@ -533,7 +536,8 @@ def run_native(args):
             line["comparator"] = comparator
         if bwd is not None:
             bwd["roofline"] = {"bound": "tensor", "achieved": bwd["value"], "peak": peaks["bf16_tflops"],
-                               "unit": UNIT, "frac": bwd["value"] / peaks["bf16_tflops"], "traffic": None,
+                               "unit": UNIT, "frac": bwd["value"] / peaks["bf16_tflops"],
+                               "traffic": load_traffic(w.name, ":bwd", BWD_KERNEL_SOURCES),
                                "peak_source": f"{peak_src} dense bf16 burst",
                                "kernels": "bwd_prep_kernel, fa_bwd_dq_kernel<%d>, fa_bwd_dkdv_kernel<%d>" % (d, d)}
             line["bwd"] = bwd
