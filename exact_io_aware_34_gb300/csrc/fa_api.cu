@@ -252,8 +252,8 @@ inline long long bwd_npad(int N) { return (static_cast<long long>(N) + 127) / 12
 
 template <int HD>
 fa_status_t bwd_launch(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
-                       void* dQ, void* dK, void* dV, int B, int H, int N, float scale, void* ws,
-                       cudaStream_t stream) {
+                       void* dQ, void* dK, void* dV, int B, int H, int N, float scale, void* ws, int drop_load,
+                       unsigned long long timeout_ns, cudaStream_t stream) {
   using C = fa::BwdCfg<HD>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -290,7 +290,8 @@ fa_status_t bwd_launch(const void* Q, const void* K, const void* V, const void* 
   p.n_blocks = static_cast<int>(npad / C::kBlk);
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
   p.scale = scale;
-  p.timeout_ns = kDefaultTimeoutNs;
+  p.timeout_ns = timeout_ns;
+  p.drop_load = drop_load;
 
   // 1. -LSE*log2(e) and -D per query row (one warp each, 8 per block)
   fa::bwd_prep_kernel<HD><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
@@ -389,9 +390,13 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N) {
   return 2 * static_cast<size_t>(B) * H * static_cast<size_t>(bwd_npad(N)) * 4;
 }
 
-fa_status_t fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
-                   void* dQ, void* dK, void* dV, int B, int H, int N, int d, float scale, void* workspace,
-                   size_t workspace_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+fa_status_t bwd_impl(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
+                     void* dQ, void* dK, void* dV, int B, int H, int N, int d, float scale, void* workspace,
+                     size_t workspace_bytes, int drop_load, unsigned long long timeout_ns, cudaStream_t stream) {
   fa_status_t st = check_args(Q, K, V, O, LSE, B, H, N, d, scale);
   if (st != FA_OK) return st;
   if (!dO || !dQ || !dK || !dV || !workspace) return FA_ERR_INVALID_ARG;
@@ -414,8 +419,29 @@ fa_status_t fa_bwd(const void* Q, const void* K, const void* V, const void* O, c
     for (int b = a + 1; b < 4; ++b)
       if (overlaps(outs[a], out_n[a], outs[b], out_n[b])) return FA_ERR_INVALID_ARG;
   }
-  if (d == 64) return bwd_launch<64>(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, scale, workspace, stream);
-  return bwd_launch<128>(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, scale, workspace, stream);
+  if (d == 64)
+    return bwd_launch<64>(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, scale, workspace, drop_load, timeout_ns, stream);
+  return bwd_launch<128>(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, scale, workspace, drop_load, timeout_ns, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status_t fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
+                   void* dQ, void* dK, void* dV, int B, int H, int N, int d, float scale, void* workspace,
+                   size_t workspace_bytes, cudaStream_t stream) {
+  return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, workspace, workspace_bytes, -1,
+                  kDefaultTimeoutNs, stream);
+}
+
+fa_status_t fa_bwd_fault_test(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                              const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int N, int d, float scale,
+                              void* workspace, size_t workspace_bytes, int drop_load, unsigned long long timeout_ns,
+                              cudaStream_t stream) {
+  if (timeout_ns == 0) return FA_ERR_INVALID_ARG;
+  return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, workspace, workspace_bytes,
+                  drop_load < 0 ? -1 : drop_load, timeout_ns, stream);
 }
 
 const char* fa_status_string(fa_status_t status) {

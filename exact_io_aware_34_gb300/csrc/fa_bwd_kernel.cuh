@@ -82,6 +82,7 @@ struct BwdParams {
   float scale_log2;       // scale * log2(e)
   float scale;
   unsigned long long timeout_ns;
+  int drop_load;          // test hook: index of a tile load to skip in each kernel, -1 = none
 };
 
 // ---------------------------------------------------------------- prep
@@ -294,6 +295,7 @@ __global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
           break;
         }
         issued = it + 1;
+        if (it == p.drop_load) continue;   // test hook: this tile never arrives
         const uint32_t fb = ptx::smem_u32(&full[slot]);
         ptx::mbar_arrive_expect_tx(fb, C::kTileBytes);
         const uint32_t dst = (is_v ? sV : sK) + slot * C::kTileBytes;
@@ -308,7 +310,7 @@ __global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
           const bool is_v = it & 1;
           const int slots = is_v ? D::kVSlots : D::kKSlots;
           const int last_j = ((issued - 1 - (is_v ? 1 : 0)) >> 1);
-          if (j + slots <= last_j) continue;
+          if (j + slots <= last_j || it == p.drop_load) continue;
           drain_wait(ptx::smem_u32(&(is_v ? bar_v_full : bar_k_full)[j % slots]), (j / slots) & 1, p.timeout_ns);
         }
       }
@@ -524,6 +526,7 @@ __global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
           break;
         }
         issued = i + 1;
+        if (i == p.drop_load) continue;    // test hook: this step's tiles never arrive
         const uint32_t full = ptx::smem_u32(&bar_in_full[slot]);
         const uint32_t dst = sRing + slot * C::kPairBytes;
         ptx::mbar_arrive_expect_tx(full, C::kPairBytes + C::kVecBytes);
@@ -540,7 +543,8 @@ __global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
       if (!ok || *abort_ptr) {
         drain_wait(kv_full, 0, p.timeout_ns);
         for (int i = issued > C::kStages ? issued - C::kStages : 0; i < issued; ++i)
-          drain_wait(ptx::smem_u32(&bar_in_full[i % C::kStages]), (i / C::kStages) & 1, p.timeout_ns);
+          if (i != p.drop_load)
+            drain_wait(ptx::smem_u32(&bar_in_full[i % C::kStages]), (i / C::kStages) & 1, p.timeout_ns);
       }
     }
     __syncwarp();

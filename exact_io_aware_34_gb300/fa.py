@@ -25,7 +25,8 @@ FA_ERR_TIMEOUT = 4
 
 #: every symbol include/fa.h declares
 EXPORTED = ("fa_fwd", "fa_get_device_status", "fa_status_string", "fa_last_cuda_error", "fa_fwd_fault_test",
-            "fa_naive_fwd", "fa_naive_workspace_bytes", "fa_naive_fwd_noalloc", "fa_bwd", "fa_bwd_workspace_bytes")
+            "fa_naive_fwd", "fa_naive_workspace_bytes", "fa_naive_fwd_noalloc", "fa_bwd", "fa_bwd_workspace_bytes",
+            "fa_bwd_fault_test")
 
 _lib = None
 
@@ -68,6 +69,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, vp, ctypes.c_size_t, vp]
     lib.fa_bwd.restype = i
+    lib.fa_bwd_fault_test.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, vp, ctypes.c_size_t, i, u64,
+                                      vp]
+    lib.fa_bwd_fault_test.restype = i
     _lib = lib
     return lib
 
@@ -209,6 +213,20 @@ def fa_bwd(q, k, v, o, do, lse, dq=None, dk=None, dv=None, scale: float | None =
     if st != FA_OK:
         raise FaError(st, "fa_bwd")
     return tuple(outs)
+
+
+def fa_bwd_fault_test(q, k, v, o, do, lse, dq, dk, dv, scale: float, workspace, drop_load: int, timeout_ns: int,
+                      stream=None) -> int:
+    """Test hook of the C ABI (see include/fa.h): returns the raw status code."""
+    _check_qkv(q, k, v)
+    B, H, N, d = q.shape
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        return int(lib.fa_bwd_fault_test(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                                         lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
+                                         float(scale), workspace.data_ptr(),
+                                         workspace.numel() * workspace.element_size(), int(drop_load),
+                                         int(timeout_ns), _stream_handle(stream, q.device)))
 
 
 def fa_fwd_fault_test(q, k, v, o, lse, scale: float, drop_load: int, timeout_ns: int, stream=None) -> int:

@@ -191,6 +191,23 @@ fa_status_t fa_fwd_fault_test(const void* Q, const void* K, const void* V, void*
                               int B, int H, int N, int d, float scale,
                               int drop_load, unsigned long long timeout_ns, cudaStream_t stream);
 
+/*
+ * fa_bwd_fault_test -- TEST HOOK, not for production use. Same as fa_bwd, but
+ * every device-side wait gives up after `timeout_ns` nanoseconds, and when
+ * `drop_load` >= 0 each backward kernel's producer skips one tile load in
+ * every CTA: in the dQ kernel the drop_load-th of K_0, V_0, K_1, V_1, ...; in
+ * the dK/dV kernel the (Q, dO) pair of query block drop_load. The waiting
+ * role then gives up, every role stops, waits for its own copies and
+ * tensor-core work in flight, frees its tensor memory and exits;
+ * fa_get_device_status reports FA_ERR_TIMEOUT and the CUDA context stays
+ * usable. dQ, dK, dV are unspecified after a drop.
+ */
+fa_status_t fa_bwd_fault_test(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                              const float* LSE, void* dQ, void* dK, void* dV,
+                              int B, int H, int N, int d, float scale,
+                              void* workspace, size_t workspace_bytes,
+                              int drop_load, unsigned long long timeout_ns, cudaStream_t stream);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif

@@ -48,3 +48,37 @@ def test_drop_beyond_last_load_is_harmless():
     lse = torch.empty(1, 1, 256, dtype=torch.float32, device="cuda")
     assert fa.fa_fwd_fault_test(q, k, v, o, lse, 0.1, 10_000, 20_000_000) == fa.FA_OK
     assert fa.fa_get_device_status()[0] == fa.FA_OK
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("drop", [0, 1, 3, 6])
+def test_backward_dropped_load_times_out_cleanly(d, drop):
+    """The same for fa_bwd: one K/V load of the dQ kernel and one Q/dO load of
+    the dK/dV kernel never arrive; both kernels end with a timeout status, and
+    the next backward call in the same context is correct."""
+    B, H, N = 1, 2, 700
+    s = 1 / math.sqrt(d)
+    q, k, v = inputs.make_random(B, H, N, d, seed=40 + drop)
+    do = inputs.make_grad(B, H, N, d, seed=40 + drop)
+    o, lse = parity.oracle_forward_inputs(q, k, v, s)
+    args = [x.cuda() for x in (q, k, v, o, do, lse)]
+    grads = [torch.zeros_like(args[0]) for _ in range(3)]
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N), dtype=torch.uint8, device="cuda")
+    st = fa.fa_bwd_fault_test(*args, *grads, s, ws, drop, 20_000_000)   # 20 ms
+    assert st == fa.FA_OK
+    st, info = fa.fa_get_device_status()
+    assert st == fa.FA_ERR_TIMEOUT, (st, info)
+    assert info[0] in (4, 5, 6, 7, 8, 9)
+    assert fa.fa_get_device_status()[0] == fa.FA_OK
+    got = parity.run_gpu_bwd(q, k, v, o, do, lse, s)
+    ref = oracle.attention_bwd(*(parity.to64(x) for x in (q, k, v, do)), s)
+    err = parity.bwd_errors(got, ref)
+    parity.assert_bwd_within(err, two_x_rule=False)
+
+
+def test_backward_fault_hook_rejects_zero_timeout():
+    q, k, v = (x.cuda() for x in inputs.make_random(1, 1, 128, 64, seed=49))
+    lse = torch.zeros(1, 1, 128, device="cuda")
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(1, 1, 128), dtype=torch.uint8, device="cuda")
+    g = [torch.zeros_like(q) for _ in range(3)]
+    assert fa.fa_bwd_fault_test(q, k, v, q.clone(), q.clone(), lse, *g, 0.125, ws, 0, 0) == fa.FA_ERR_INVALID_ARG
