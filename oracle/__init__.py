@@ -14,3 +14,9 @@ from .backward import (  # noqa: F401
     attention_bwd_recompute,
     naive_bf16_attention_bwd,
 )
+from .gqa import (  # noqa: F401
+    attention_gqa,
+    attention_gqa_rows,
+    attention_split,
+    merge_partials,
+)
