@@ -10,12 +10,14 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
 
 #include "../../include/fa.h"
 #include "fa_bwd_kernel.cuh"
+#include "fa_decode_kernel.cuh"
 #include "fa_fwd_kernel.cuh"
 #include "naive_kernels.cuh"
 
@@ -76,8 +78,8 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 }
 
 template <int HD>
-fa_status_t launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N,
-                   float scale, int drop_load, unsigned long long timeout_ns, cudaStream_t stream) {
+fa_status_t launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int H_kv, int N,
+                   int N_kv, float scale, int drop_load, unsigned long long timeout_ns, cudaStream_t stream) {
   using C = fa::FwdCfg<HD>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -93,16 +95,18 @@ fa_status_t launch(const void* Q, const void* K, const void* V, void* O, float* 
   if (attr_err[dev] != cudaSuccess) return cuda_fail(attr_err[dev]);
 
   CUtensorMap mq, mk, mv;
-  const int BH = B * H;
-  if (!make_map(&mq, Q, BH, N, HD) || !make_map(&mk, K, BH, N, HD) || !make_map(&mv, V, BH, N, HD))
+  if (!make_map(&mq, Q, B * H, N, HD) || !make_map(&mk, K, B * H_kv, N_kv, HD) ||
+      !make_map(&mv, V, B * H_kv, N_kv, HD))
     return cuda_fail(cudaErrorInvalidValue);
 
   fa::FwdParams p;
   p.O = static_cast<__nv_bfloat16*>(O);
   p.LSE = LSE;
   p.N = N;
+  p.N_kv = N_kv;
   p.H = H;
-  p.n_kv_blocks = (N + C::kBN - 1) / C::kBN;
+  p.H_kv = H_kv;
+  p.n_kv_blocks = (N_kv + C::kBN - 1) / C::kBN;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
   p.timeout_ns = timeout_ns;
   p.drop_load = drop_load;
@@ -132,8 +136,8 @@ fa_status_t fwd_impl(const void* Q, const void* K, const void* V, void* O, float
     if (overlaps(O, n_qkv, in, n_qkv) || overlaps(LSE, n_lse, in, n_qkv)) return FA_ERR_INVALID_ARG;
   }
   if (overlaps(O, n_qkv, LSE, n_lse)) return FA_ERR_INVALID_ARG;
-  if (d == 64) return launch<64>(Q, K, V, O, LSE, B, H, N, scale, drop_load, timeout_ns, stream);
-  return launch<128>(Q, K, V, O, LSE, B, H, N, scale, drop_load, timeout_ns, stream);
+  if (d == 64) return launch<64>(Q, K, V, O, LSE, B, H, H, N, N, scale, drop_load, timeout_ns, stream);
+  return launch<128>(Q, K, V, O, LSE, B, H, H, N, N, scale, drop_load, timeout_ns, stream);
 }
 
 // ---------------------------------------------------------------- standard attention
@@ -424,9 +428,198 @@ fa_status_t bwd_impl(const void* Q, const void* K, const void* V, const void* O,
   return bwd_launch<128>(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, scale, workspace, drop_load, timeout_ns, stream);
 }
 
+// ---------------------------------------------------------------- shared K/V heads, short queries
+struct KvPlan {
+  int G, hp, tiles_per_group, n_kv_blocks, blocks_per_split, num_splits;
+};
+
+int device_sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return 148;
+  return sms;
+}
+
+// Packing and key split of the short-query path (N_q <= 128). With
+// num_splits <= 0 the split count fills one wave of CTAs (one per SM); it
+// is capped by the number of key blocks, and ranges are whole blocks with
+// no empty range.
+KvPlan kv_plan(int B, int H, int H_kv, int N_q, int N_kv, int num_splits) {
+  KvPlan k;
+  k.G = H / H_kv;
+  k.hp = std::min(k.G, 128 / N_q);
+  k.tiles_per_group = (k.G + k.hp - 1) / k.hp;
+  k.n_kv_blocks = (N_kv + 127) / 128;
+  int s = num_splits;
+  if (s <= 0) {
+    const long long base = static_cast<long long>(B) * H_kv * k.tiles_per_group;
+    const int sms = device_sm_count();
+    s = base >= sms ? 1 : static_cast<int>(sms / base);
+  }
+  s = std::max(1, std::min(s, k.n_kv_blocks));
+  k.blocks_per_split = (k.n_kv_blocks + s - 1) / s;
+  k.num_splits = (k.n_kv_blocks + k.blocks_per_split - 1) / k.blocks_per_split;
+  return k;
+}
+
+size_t kv_workspace_bytes(int B, int H, int N_q, int d, const KvPlan& k) {
+  if (k.num_splits <= 1) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * N_q;
+  return static_cast<size_t>(k.num_splits) * rows * (d + 1) * 4;
+}
+
+fa_status_t kv_check(const void* Q, const void* K, const void* V, const void* O, const float* LSE, int B, int H,
+                     int H_kv, int N_q, int N_kv, int d, float scale) {
+  if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || H_kv < 1 || N_q < 1 || N_kv < 1 || d < 1) return FA_ERR_INVALID_ARG;
+  if (B > 65535 || H > 65535 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H * N_q >= (1LL << 31) || static_cast<long long>(B) * H_kv * N_kv >= (1LL << 31))
+    return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (scale < 0.f) return FA_ERR_UNSUPPORTED;
+  for (const void* ptr : {Q, K, V, O})
+    if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return FA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(LSE) % 4 != 0) return FA_ERR_INVALID_ARG;
+  const size_t n_q = static_cast<size_t>(B) * H * N_q * d * 2;
+  const size_t n_kv = static_cast<size_t>(B) * H_kv * N_kv * d * 2;
+  const size_t n_lse = static_cast<size_t>(B) * H * N_q * 4;
+  if (overlaps(O, n_q, Q, n_q) || overlaps(O, n_q, K, n_kv) || overlaps(O, n_q, V, n_kv)) return FA_ERR_INVALID_ARG;
+  if (overlaps(LSE, n_lse, Q, n_q) || overlaps(LSE, n_lse, K, n_kv) || overlaps(LSE, n_lse, V, n_kv) ||
+      overlaps(LSE, n_lse, O, n_q))
+    return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+template <int HD>
+fa_status_t decode_launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int H_kv,
+                          int N_q, int N_kv, float scale, const KvPlan& k, void* ws, int drop_load,
+                          unsigned long long timeout_ns, cudaStream_t stream) {
+  using C = fa::DecCfg<HD>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= 64) return FA_ERR_UNSUPPORTED;
+  static std::once_flag once[64];
+  static cudaError_t attr_err[64];
+  std::call_once(once[dev], [&] {
+    attr_err[dev] =
+        cudaFuncSetAttribute(fa::fa_decode_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  });
+  if (attr_err[dev] != cudaSuccess) return cuda_fail(attr_err[dev]);
+
+  // Q as [B*H][N_q][d] with a box of 64 x N_q rows x hp heads: one load
+  // brings the packed rows of hp query heads. K, V as [B*H_kv][N_kv][d].
+  CUtensorMap mq, mk, mv;
+  auto fn = encode_fn();
+  if (!fn) return cuda_fail(cudaErrorInvalidValue);
+  {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(N_q),
+                          static_cast<cuuint64_t>(B) * H};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(HD) * 2, static_cast<cuuint64_t>(N_q) * HD * 2};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(N_q), static_cast<cuuint32_t>(k.hp)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (fn(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(Q), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cuda_fail(cudaErrorInvalidValue);
+  }
+  if (!make_map(&mk, K, B * H_kv, N_kv, HD) || !make_map(&mv, V, B * H_kv, N_kv, HD))
+    return cuda_fail(cudaErrorInvalidValue);
+
+  fa::DecParams p;
+  const size_t rows = static_cast<size_t>(B) * H * N_q;
+  p.O = static_cast<__nv_bfloat16*>(O);
+  p.LSE = LSE;
+  p.O_part = k.num_splits > 1 ? static_cast<float*>(ws) : nullptr;
+  p.LSE_part = k.num_splits > 1 ? static_cast<float*>(ws) + static_cast<size_t>(k.num_splits) * rows * HD : nullptr;
+  p.N_q = N_q;
+  p.N_kv = N_kv;
+  p.H = H;
+  p.H_kv = H_kv;
+  p.G = k.G;
+  p.hp = k.hp;
+  p.tiles_per_group = k.tiles_per_group;
+  p.n_kv_blocks = k.n_kv_blocks;
+  p.blocks_per_split = k.blocks_per_split;
+  p.num_splits = k.num_splits;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  p.timeout_ns = timeout_ns;
+  p.drop_load = drop_load;
+  const dim3 grid(static_cast<unsigned>(k.tiles_per_group * k.num_splits), H_kv, B);
+  fa::fa_decode_kernel<HD><<<grid, C::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (k.num_splits > 1) {
+    fa::decode_merge_kernel<HD><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
+        p.O_part, p.LSE_part, static_cast<__nv_bfloat16*>(O), LSE, static_cast<long long>(rows), k.num_splits);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return FA_OK;
+}
+
+fa_status_t kv_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int H_kv,
+                    int N_q, int N_kv, int d, float scale, int num_splits, void* workspace, size_t workspace_bytes,
+                    int drop_load, unsigned long long timeout_ns, cudaStream_t stream) {
+  fa_status_t st = kv_check(Q, K, V, O, LSE, B, H, H_kv, N_q, N_kv, d, scale);
+  if (st != FA_OK) return st;
+  if (N_q > 128) {
+    // Long query blocks: the fused forward kernel with the K/V head mapping.
+    if (num_splits > 1) return FA_ERR_UNSUPPORTED;
+    if (d == 64) return launch<64>(Q, K, V, O, LSE, B, H, H_kv, N_q, N_kv, scale, drop_load, timeout_ns, stream);
+    return launch<128>(Q, K, V, O, LSE, B, H, H_kv, N_q, N_kv, scale, drop_load, timeout_ns, stream);
+  }
+  const KvPlan k = kv_plan(B, H, H_kv, N_q, N_kv, num_splits);
+  const size_t need = kv_workspace_bytes(B, H, N_q, d, k);
+  if (need > 0) {
+    if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 128 != 0 || workspace_bytes < need)
+      return FA_ERR_INVALID_ARG;
+    const size_t n_q = static_cast<size_t>(B) * H * N_q * d * 2;
+    const size_t n_kv = static_cast<size_t>(B) * H_kv * N_kv * d * 2;
+    if (overlaps(workspace, need, Q, n_q) || overlaps(workspace, need, K, n_kv) ||
+        overlaps(workspace, need, V, n_kv) || overlaps(workspace, need, O, n_q) ||
+        overlaps(workspace, need, LSE, static_cast<size_t>(B) * H * N_q * 4))
+      return FA_ERR_INVALID_ARG;
+  }
+  if (d == 64)
+    return decode_launch<64>(Q, K, V, O, LSE, B, H, H_kv, N_q, N_kv, scale, k, workspace, drop_load, timeout_ns,
+                             stream);
+  return decode_launch<128>(Q, K, V, O, LSE, B, H, H_kv, N_q, N_kv, scale, k, workspace, drop_load, timeout_ns,
+                            stream);
+}
+
 }  // namespace
 
 extern "C" {
+
+int fa_fwd_kv_num_splits(int B, int H, int H_kv, int N_q, int N_kv, int d) {
+  if (B < 1 || H < 1 || H_kv < 1 || H % H_kv != 0 || N_q < 1 || N_kv < 1 || (d != 64 && d != 128)) return 0;
+  if (N_q > 128) return 1;
+  return kv_plan(B, H, H_kv, N_q, N_kv, 0).num_splits;
+}
+
+size_t fa_fwd_kv_workspace_bytes(int B, int H, int H_kv, int N_q, int N_kv, int d, int num_splits) {
+  if (B < 1 || H < 1 || H_kv < 1 || H % H_kv != 0 || N_q < 1 || N_kv < 1 || (d != 64 && d != 128)) return 0;
+  if (N_q > 128) return 0;
+  return kv_workspace_bytes(B, H, N_q, d, kv_plan(B, H, H_kv, N_q, N_kv, num_splits));
+}
+
+fa_status_t fa_fwd_kv(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int H_kv,
+                      int N_q, int N_kv, int d, float scale, int num_splits, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream) {
+  return kv_impl(Q, K, V, O, LSE, B, H, H_kv, N_q, N_kv, d, scale, num_splits, workspace, workspace_bytes, -1,
+                 kDefaultTimeoutNs, stream);
+}
+
+fa_status_t fa_fwd_kv_fault_test(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+                                 int H_kv, int N_q, int N_kv, int d, float scale, int num_splits, void* workspace,
+                                 size_t workspace_bytes, int drop_load, unsigned long long timeout_ns,
+                                 cudaStream_t stream) {
+  if (timeout_ns == 0) return FA_ERR_INVALID_ARG;
+  return kv_impl(Q, K, V, O, LSE, B, H, H_kv, N_q, N_kv, d, scale, num_splits, workspace, workspace_bytes,
+                 drop_load < 0 ? -1 : drop_load, timeout_ns, stream);
+}
 
 fa_status_t fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
                    void* dQ, void* dK, void* dV, int B, int H, int N, int d, float scale, void* workspace,

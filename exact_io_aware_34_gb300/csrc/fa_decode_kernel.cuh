@@ -1,0 +1,428 @@
+// Exact attention for short query blocks against long key/value sequences
+// with shared K/V heads: the decode (generation) shape. sm_103a, tcgen05 +
+// TMEM + TMA.
+//
+// What is computed is the forward's definition: for query head h and K/V
+// head h / G (G = H / H_kv query heads share one K/V head, the grouping of
+// "FlashAttention：IO 感知的精确注意力", "与其他知识点的关系"),
+// O = softmax(scale Q K^T) V and LSE per query row, every query row
+// attending to all N_kv keys.
+//
+// Decode is bandwidth-bound ("常见误区" on the same page): the K/V bytes
+// dominate. Two things keep all SMs streaming them:
+//  * Packing. The query rows of the G heads that share a K/V head fill one
+//    128-row tile (hp = min(G, 128 / N_q) heads of N_q rows each; one TMA box
+//    {64, N_q, hp} loads them), so each K/V tile is read once per group
+//    rather than once per query head.
+//  * Split keys. The key blocks of a (b, K/V head, tile) are cut into
+//    num_splits contiguous ranges, one CTA each. A CTA's partial result over
+//    its range (O normalised by its own l, and its LSE) goes to a float32
+//    workspace, and decode_merge_kernel combines the partials with the
+//    online-softmax rule of "Flash Attention (FA1)", derivation steps 4-5:
+//    LSE = ln sum_s e^{LSE_s}, O = sum_s e^{LSE_s - LSE} O_s.
+//    With one split the CTA writes O and LSE directly.
+//
+// Per CTA (192 threads): warps 0-3 run the softmax and epilogue of the one
+// tile (one thread per row), warp 4 is the TMA producer, warp 5 allocates
+// TMEM and issues the MMAs. TMEM: S at column 0 (P, packed bf16, over its
+// first 64 columns), O at column 128. The per-block update is the forward
+// kernel's, including the lazy rescale.
+#pragma once
+
+#include "fa_fwd_kernel.cuh"
+
+namespace fa {
+
+enum : unsigned int { kRoleDecProducer = 10, kRoleDecMma = 11, kRoleDecSoftmax = 12 };
+
+template <int HD>
+struct DecCfg {
+  static constexpr int kBM = 128;
+  static constexpr int kBN = 128;
+  static constexpr int kChunks = HD / 64;
+  static constexpr int kChunkBytes = 128 * 128;
+  static constexpr int kTileBytes = kChunks * kChunkBytes;
+  static constexpr int kStages = (HD == 128) ? 6 : 12;     // K/V ring slots
+  static constexpr int kSmemBytes = kTileBytes + kStages * kTileBytes + 1024;
+  static constexpr int kThreads = 192;
+  static constexpr uint32_t kTmemCols = 256;
+  static constexpr uint32_t kColS = 0;
+  static constexpr uint32_t kColO = 128;
+  static constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(kBM, kBN, false, false);
+  static constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kBM, HD, false, true);
+};
+
+struct DecParams {
+  __nv_bfloat16* O;       // [B, H, N_q, d] (num_splits == 1)
+  float* LSE;             // [B, H, N_q]    (num_splits == 1)
+  float* O_part;          // [num_splits][B*H*N_q][d] (num_splits > 1)
+  float* LSE_part;        // [num_splits][B*H*N_q]
+  int N_q;
+  int N_kv;
+  int H;
+  int H_kv;
+  int G;                  // H / H_kv
+  int hp;                 // query heads packed per tile
+  int tiles_per_group;    // ceil(G / hp)
+  int n_kv_blocks;
+  int blocks_per_split;
+  int num_splits;
+  float scale_log2;
+  unsigned long long timeout_ns;
+  int drop_load;          // test hook: index of a K/V load (within a CTA's range) to skip, -1 = none
+};
+
+template <int HD>
+__global__ void __launch_bounds__(DecCfg<HD>::kThreads, 1)
+    fa_decode_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const DecParams p) {
+  using C = DecCfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_q_full;
+  __shared__ __align__(8) uint64_t bar_kv_full[C::kStages];
+  __shared__ __align__(8) uint64_t bar_kv_empty[C::kStages];
+  __shared__ __align__(8) uint64_t bar_s_full;
+  __shared__ __align__(8) uint64_t bar_p_full;
+  __shared__ __align__(8) uint64_t bar_o_full;
+  __shared__ __align__(8) uint64_t bar_drain;
+  __shared__ uint32_t tmem_base_slot;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int tile = blockIdx.x / p.num_splits;
+  const int split = blockIdx.x - tile * p.num_splits;
+  const int kvh = blockIdx.y;
+  const int b = blockIdx.z;
+  const int g0 = tile * p.hp;                                   // first query head of the group in this tile
+  const int nh = min(p.hp, p.G - g0);                           // query heads in this tile
+  const int rows = nh * p.N_q;                                  // tile rows that are real
+  const int j0 = split * p.blocks_per_split;
+  const int j1 = min(p.n_kv_blocks, j0 + p.blocks_per_split);
+  const int n = j1 - j0;                                        // key blocks of this CTA (>= 1)
+  const int bh_kv = b * p.H_kv + kvh;
+  const int bh_q0 = b * p.H + kvh * p.G + g0;                   // first query head, flattened
+
+  const uint32_t smem_base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sQ = smem_base;
+  const uint32_t sKV = smem_base + C::kTileBytes;
+  uint8_t* q_generic = smem_raw + (sQ - ptx::smem_u32(smem_raw));
+
+  // Rows of the Q tile that no query fills are zero, so that their scores are
+  // finite; they are never stored.
+  const int box_rows = p.hp * p.N_q;
+  for (int c = 0; c < C::kChunks; ++c)
+    for (int i = threadIdx.x; i < (C::kBM - box_rows) * 8; i += C::kThreads)
+      reinterpret_cast<uint4*>(q_generic + c * C::kChunkBytes + box_rows * 128)[i] = make_uint4(0u, 0u, 0u, 0u);
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_u32(&bar_q_full), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&bar_kv_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bar_kv_empty[s]), 1);
+    }
+    ptx::mbar_init(ptx::smem_u32(&bar_s_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&bar_p_full), C::kBM);
+    ptx::mbar_init(ptx::smem_u32(&bar_o_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&bar_drain), 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 5) {
+    ptx::tmem_alloc(ptx::smem_u32(&tmem_base_slot), C::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (warp == 4 && lane == 0) {
+    ptx::prefetch_tmap(&tmQ);
+    ptx::prefetch_tmap(&tmK);
+    ptx::prefetch_tmap(&tmV);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = tmem_base_slot;
+  volatile int* abort_ptr = &abort_flag;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_q = ptx::policy_evict_first();
+      const uint64_t pol_kv = ptx::policy_evict_first();   // each K/V tile is read by one CTA
+      const uint32_t q_full = ptx::smem_u32(&bar_q_full);
+      ptx::mbar_arrive_expect_tx(q_full, C::kChunks * 128 * box_rows);
+      for (int c = 0; c < C::kChunks; ++c)
+        ptx::tma_load_3d(sQ + c * C::kChunkBytes, &tmQ, q_full, c * 64, 0, bh_q0, pol_q);
+      int issued = 0;
+      bool ok = true;
+      for (int jj = 0; jj < n && ok; ++jj) {
+        for (int kv = 0; kv < 2; ++kv) {
+          const int it = 2 * jj + kv;
+          const int slot = it % C::kStages;
+          if (!wait_or_abort(ptx::smem_u32(&bar_kv_empty[slot]), ((it / C::kStages) & 1) ^ 1u, abort_ptr,
+                             p.timeout_ns, kRoleDecProducer)) {
+            ok = false;
+            break;
+          }
+          issued = it + 1;
+          if (it == p.drop_load) continue;   // test hook: this tile never arrives
+          const uint32_t full = ptx::smem_u32(&bar_kv_full[slot]);
+          ptx::mbar_arrive_expect_tx(full, C::kTileBytes);
+          const void* map = kv ? static_cast<const void*>(&tmV) : static_cast<const void*>(&tmK);
+          for (int c = 0; c < C::kChunks; ++c)
+            ptx::tma_load_3d(sKV + slot * C::kTileBytes + c * C::kChunkBytes, map, full, c * 64,
+                             (j0 + jj) * C::kBN, bh_kv, pol_kv);
+        }
+      }
+      if (!ok || *abort_ptr) {
+        drain_wait(q_full, 0, p.timeout_ns);
+        for (int it = issued > C::kStages ? issued - C::kStages : 0; it < issued; ++it)
+          if (it != p.drop_load)
+            drain_wait(ptx::smem_u32(&bar_kv_full[it % C::kStages]), (it / C::kStages) & 1, p.timeout_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      auto kv_wait = [&](int it) {
+        return wait_or_abort(ptx::smem_u32(&bar_kv_full[it % C::kStages]), (it / C::kStages) & 1, abort_ptr,
+                             p.timeout_ns, kRoleDecMma);
+      };
+      bool ok = wait_or_abort(ptx::smem_u32(&bar_q_full), 0, abort_ptr, p.timeout_ns, kRoleDecMma);
+      for (int jj = 0; jj < n && ok; ++jj) {
+        if (jj > 0) {
+          // O += P V for the previous block (P sits in the S columns).
+          ok = wait_or_abort(ptx::smem_u32(&bar_p_full), (jj - 1) & 1, abort_ptr, p.timeout_ns, kRoleDecMma);
+          if (ok) ok = kv_wait(2 * (jj - 1) + 1);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          const uint32_t v_tile = sKV + ((2 * (jj - 1) + 1) % C::kStages) * C::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < C::kBN / 16; ++kk)
+            ptx::mma_ts(tmem_base + C::kColO, tmem_base + C::kColS + kk * 8,
+                        ptx::desc_mnmajor_sw128(v_tile + kk * 16 * 128, C::kChunkBytes), C::kIdescPV,
+                        (jj > 1 || kk > 0) ? 1u : 0u);
+          ptx::mma_commit(ptx::smem_u32(&bar_kv_empty[(2 * (jj - 1) + 1) % C::kStages]));
+        }
+        ok = kv_wait(2 * jj);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const uint32_t k_tile = sKV + ((2 * jj) % C::kStages) * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+          ptx::mma_ss(tmem_base + C::kColS, ptx::desc_kmajor_sw128(sQ + off), ptx::desc_kmajor_sw128(k_tile + off),
+                      C::kIdescQK, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(ptx::smem_u32(&bar_s_full));
+        ptx::mma_commit(ptx::smem_u32(&bar_kv_empty[(2 * jj) % C::kStages]));
+      }
+      if (ok) {
+        // The last block's P V.
+        ok = wait_or_abort(ptx::smem_u32(&bar_p_full), (n - 1) & 1, abort_ptr, p.timeout_ns, kRoleDecMma);
+        if (ok) ok = kv_wait(2 * (n - 1) + 1);
+        if (ok) {
+          ptx::tc_fence_after();
+          const uint32_t v_tile = sKV + ((2 * (n - 1) + 1) % C::kStages) * C::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < C::kBN / 16; ++kk)
+            ptx::mma_ts(tmem_base + C::kColO, tmem_base + C::kColS + kk * 8,
+                        ptx::desc_mnmajor_sw128(v_tile + kk * 16 * 128, C::kChunkBytes), C::kIdescPV,
+                        (n > 1 || kk > 0) ? 1u : 0u);
+          ptx::mma_commit(ptx::smem_u32(&bar_o_full));
+          ptx::mma_commit(ptx::smem_u32(&bar_kv_empty[(2 * (n - 1) + 1) % C::kStages]));
+        }
+      }
+      if (!ok) {
+        ptx::mma_commit(ptx::smem_u32(&bar_drain));
+        drain_wait(ptx::smem_u32(&bar_drain), 0, p.timeout_ns);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int quarter = warp;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem_base + lane_addr + C::kColS;
+    const uint32_t tO = tmem_base + lane_addr + C::kColO;
+    const float sl2 = p.scale_log2;
+    float m_use = 0.f;
+    float l = 0.f;
+    bool ok = true;
+    for (int jj = 0; jj < n; ++jj) {
+      ok = wait_warp_or_abort(ptx::smem_u32(&bar_s_full), jj & 1, abort_ptr, p.timeout_ns, kRoleDecSoftmax);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      uint32_t s[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + 32 * c, s[c]);
+      ptx::tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) ptx::reg_fence32(s[c]);
+
+      const int valid = p.N_kv - (j0 + jj) * C::kBN;   // keys of this block that exist
+      const bool ragged = valid < C::kBN;
+      if (ragged) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (32 * c + i >= valid) s[c][i] = __float_as_uint(-INFINITY);
+      }
+      float mc[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int c = k >> 1, bb = (k & 1) * 16;
+        mc[k] = fmaxf(__uint_as_float(s[c][bb]), __uint_as_float(s[c][bb + 1]));
+#pragma unroll
+        for (int i = 2; i < 16; i += 2)
+          mc[k] = ptx::max3(mc[k], __uint_as_float(s[c][bb + i]), __uint_as_float(s[c][bb + i + 1]));
+      }
+      const float mt = ptx::max3(ptx::max3(mc[0], mc[1], mc[2]), ptx::max3(mc[3], mc[4], mc[5]),
+                                 fmaxf(mc[6], mc[7]));
+      float alpha = 1.f;
+      bool rescale_o = false;
+      if (jj == 0) {
+        m_use = mt;
+      } else {
+        const bool need = (mt - m_use) * sl2 > kRescaleLog2;
+        rescale_o = __any_sync(0xffffffffu, need);
+        if (need) {
+          alpha = ptx::ex2_approx((m_use - mt) * sl2);
+          m_use = mt;
+        }
+      }
+      const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
+      const float neg_m = -m_use * sl2;
+      const uint64_t negmx2 = ptx::f2_pack(neg_m, neg_m);
+      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+      uint32_t pk[2][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          float x0, x1;
+          ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[c][i]), __uint_as_float(s[c][i + 1])), sl2x2,
+                                     negmx2),
+                         x0, x1);
+          float p0 = ptx::ex2_approx(x0);
+          float p1 = ptx::ex2_approx(x1);
+          if (ragged) {
+            if (32 * c + i >= valid) p0 = 0.f;
+            if (32 * c + i + 1 >= valid) p1 = 0.f;
+          }
+          acc[(i >> 1) & 3] = ptx::f2_add(acc[(i >> 1) & 3], ptx::f2_pack(p0, p1));
+          pk[c >> 1][(c & 1) * 16 + (i >> 1)] = ptx::pack_bf16x2(p0, p1);
+        }
+      }
+      float sum;
+      {
+        float a0, a1, b0, b1;
+        ptx::f2_unpack(ptx::f2_add(acc[0], acc[1]), a0, a1);
+        ptx::f2_unpack(ptx::f2_add(acc[2], acc[3]), b0, b1);
+        sum = (a0 + a1) + (b0 + b1);
+      }
+      l = l * alpha + sum;
+      ptx::tmem_st32(tS, pk[0]);
+      ptx::tmem_st32(tS + 32, pk[1]);
+      if (rescale_o) {
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t o[32];
+          ptx::tmem_ld32(tO + 32 * c, o);
+          ptx::tmem_ld_wait();
+          ptx::reg_fence32(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          ptx::tmem_st32(tO + 32 * c, o);
+        }
+      }
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(ptx::smem_u32(&bar_p_full));
+    }
+    if (ok) ok = wait_warp_or_abort(ptx::smem_u32(&bar_o_full), 0, abort_ptr, p.timeout_ns, kRoleDecSoftmax);
+    if (ok) {
+      ptx::tc_fence_after();
+      // Row r of the tile is query row r % N_q of query head g0 + r / N_q.
+      const bool in_range = row < rows;
+      const int hq = row / p.N_q;
+      const size_t grow = (static_cast<size_t>(bh_q0) + hq) * p.N_q + (row - hq * p.N_q);
+      const float inv_l = 1.f / l;
+      const float lse = (m_use * sl2 + __log2f(l)) * 0.69314718055994530942f;
+      const size_t n_rows = static_cast<size_t>(gridDim.z) * p.H * p.N_q;
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t o[32];
+        ptx::tmem_ld32(tO + 32 * c, o);
+        ptx::tmem_ld_wait();
+        ptx::reg_fence32(o);
+        if (!in_range) continue;
+        if (p.num_splits == 1) {
+          uint32_t packed[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            packed[i] = ptx::pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+          uint4* dst = reinterpret_cast<uint4*>(p.O + grow * HD + 32 * c);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+        } else {
+          float4* dst = reinterpret_cast<float4*>(p.O_part + (split * n_rows + grow) * HD + 32 * c);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
+                                 __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
+        }
+      }
+      if (in_range) {
+        if (p.num_splits == 1) p.LSE[grow] = lse;
+        else p.LSE_part[split * n_rows + grow] = lse;
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+// One warp per query row: combine the num_splits partial results of the row.
+// LSE = m + ln sum_s e^{LSE_s - m} with m = max_s LSE_s, and
+// O = sum_s e^{LSE_s - LSE} O_s, rounded once to bf16.
+template <int HD>
+__global__ void __launch_bounds__(256) decode_merge_kernel(const float* __restrict__ O_part,
+                                                           const float* __restrict__ LSE_part,
+                                                           __nv_bfloat16* __restrict__ O, float* __restrict__ LSE,
+                                                           long long n_rows, int num_splits) {
+  const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (row >= n_rows) return;
+  float m = -INFINITY;
+  for (int s = 0; s < num_splits; ++s) m = fmaxf(m, LSE_part[s * n_rows + row]);
+  constexpr int kPer = HD / 32;     // output elements per lane: 4 or 2
+  float acc[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+  float total = 0.f;
+  for (int s = 0; s < num_splits; ++s) {
+    const float w = __expf(LSE_part[s * n_rows + row] - m);
+    total += w;
+    const float* src = O_part + (s * n_rows + row) * HD + lane * kPer;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) acc[e] = fmaf(w, src[e], acc[e]);
+  }
+  const float inv = 1.f / total;
+  __nv_bfloat16* dst = O + row * HD + lane * kPer;
+#pragma unroll
+  for (int e = 0; e < kPer; e += 2)
+    *reinterpret_cast<__nv_bfloat162*>(dst + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+  if (lane == 0) LSE[row] = m + __logf(total);
+}
+
+}  // namespace fa

@@ -76,8 +76,10 @@ struct FwdCfg {
 struct FwdParams {
   __nv_bfloat16* O;
   float* LSE;
-  int N;
-  int H;
+  int N;                       // query rows per head (rows of Q, O, LSE)
+  int N_kv;                    // keys per K/V head
+  int H;                       // query heads
+  int H_kv;                    // K/V heads; query head h reads K/V head h / (H / H_kv)
   int n_kv_blocks;
   float scale_log2;            // scale * log2(e)
   unsigned long long timeout_ns;
@@ -168,6 +170,7 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int bh = blockIdx.z * p.H + blockIdx.y;
+  const int bh_kv = blockIdx.z * p.H_kv + blockIdx.y / (p.H / p.H_kv);
   const int q_row0 = blockIdx.x * (C::kQTiles * C::kBM);
   const int n_kv = p.n_kv_blocks;
 
@@ -237,7 +240,7 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
           const void* map = kv ? static_cast<const void*>(&tmV) : static_cast<const void*>(&tmK);
           for (int c = 0; c < C::kChunks; ++c)
             ptx::tma_load_3d(sKV + slot * C::kTileBytes + c * C::kChunkBytes, map, full, c * 64,
-                             j * C::kBN, bh, pol_kv);
+                             j * C::kBN, bh_kv, pol_kv);
         }
       }
       if (!ok || *abort_ptr) {
@@ -353,7 +356,7 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) ptx::reg_fence32(s[c]);
 
-      const int valid = p.N - j * C::kBN;    // keys of this block that exist
+      const int valid = p.N_kv - j * C::kBN;    // keys of this block that exist
       const bool ragged = valid < C::kBN;
       if (ragged) {
 #pragma unroll

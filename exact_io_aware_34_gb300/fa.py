@@ -26,7 +26,8 @@ FA_ERR_TIMEOUT = 4
 #: every symbol include/fa.h declares
 EXPORTED = ("fa_fwd", "fa_get_device_status", "fa_status_string", "fa_last_cuda_error", "fa_fwd_fault_test",
             "fa_naive_fwd", "fa_naive_workspace_bytes", "fa_naive_fwd_noalloc", "fa_bwd", "fa_bwd_workspace_bytes",
-            "fa_bwd_fault_test")
+            "fa_bwd_fault_test", "fa_fwd_kv", "fa_fwd_kv_num_splits", "fa_fwd_kv_workspace_bytes",
+            "fa_fwd_kv_fault_test")
 
 _lib = None
 
@@ -72,6 +73,14 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_bwd_fault_test.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, vp, ctypes.c_size_t, i, u64,
                                       vp]
     lib.fa_bwd_fault_test.restype = i
+    lib.fa_fwd_kv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, ctypes.c_size_t, vp]
+    lib.fa_fwd_kv.restype = i
+    lib.fa_fwd_kv_fault_test.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, ctypes.c_size_t, i, u64, vp]
+    lib.fa_fwd_kv_fault_test.restype = i
+    lib.fa_fwd_kv_num_splits.argtypes = [i, i, i, i, i, i]
+    lib.fa_fwd_kv_num_splits.restype = i
+    lib.fa_fwd_kv_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
+    lib.fa_fwd_kv_workspace_bytes.restype = ctypes.c_size_t
     _lib = lib
     return lib
 
@@ -167,6 +176,72 @@ def fa_naive_fwd(q, k, v, o=None, lse=None, scale: float | None = None, workspac
     if st != FA_OK:
         raise FaError(st, "fa_naive_fwd")
     return o, lse
+
+
+def fa_fwd_kv_num_splits(B: int, H: int, H_kv: int, N_q: int, N_kv: int, d: int) -> int:
+    return int(load_library().fa_fwd_kv_num_splits(int(B), int(H), int(H_kv), int(N_q), int(N_kv), int(d)))
+
+
+def fa_fwd_kv_workspace_bytes(B: int, H: int, H_kv: int, N_q: int, N_kv: int, d: int, num_splits: int = 0) -> int:
+    return int(load_library().fa_fwd_kv_workspace_bytes(int(B), int(H), int(H_kv), int(N_q), int(N_kv), int(d),
+                                                         int(num_splits)))
+
+
+def _check_kv(q, k, v):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 4 \
+                or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor [B, heads, N, d]")
+    if k.shape != v.shape or q.shape[0] != k.shape[0] or q.shape[3] != k.shape[3]:
+        raise ValueError(f"shapes do not match: q {tuple(q.shape)} k {tuple(k.shape)} v {tuple(v.shape)}")
+    if not (q.device == k.device == v.device):
+        raise ValueError("q, k, v must be on the same device")
+
+
+def fa_fwd_kv(q, k, v, o=None, lse=None, scale: float | None = None, num_splits: int = 0, workspace=None,
+              stream=None):
+    """O = softmax(scale q k^T) v with shared K/V heads and any N_q, N_kv.
+
+    q: bf16 [B, H, N_q, d]; k, v: bf16 [B, H_kv, N_kv, d] with H a multiple of
+    H_kv (query head h uses K/V head h // (H // H_kv)). Returns (o, lse).
+    ``num_splits`` = 0 lets the library choose the key split for N_q <= 128;
+    the workspace is allocated with torch when needed and not given.
+    """
+    _check_kv(q, k, v)
+    B, H, N_q, d = q.shape
+    H_kv, N_kv = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N_q), dtype=torch.float32, device=q.device)
+    need = fa_fwd_kv_workspace_bytes(B, H, H_kv, N_q, N_kv, d, num_splits)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.fa_fwd_kv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, H_kv, N_q,
+                           N_kv, d, float(scale), int(num_splits), ws_ptr, ws_bytes, _stream_handle(stream, q.device))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_kv")
+    return o, lse
+
+
+def fa_fwd_kv_fault_test(q, k, v, o, lse, scale: float, num_splits: int, workspace, drop_load: int,
+                         timeout_ns: int, stream=None) -> int:
+    """Test hook of the C ABI (see include/fa.h): returns the raw status code."""
+    _check_kv(q, k, v)
+    B, H, N_q, d = q.shape
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        return int(lib.fa_fwd_kv_fault_test(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, k.shape[1], N_q, k.shape[2],
+            d, float(scale), int(num_splits), workspace.data_ptr() if workspace is not None else None,
+            workspace.numel() * workspace.element_size() if workspace is not None else 0, int(drop_load),
+            int(timeout_ns), _stream_handle(stream, q.device)))
 
 
 def fa_bwd_workspace_bytes(B: int, H: int, N: int) -> int:

@@ -7,6 +7,8 @@ side (tests, bench) use, so that both see the identical bf16 bits.
 Recipe (the pages name no dataset; every input is synthetic):
   * the backward pass's incoming gradient dO: standard normal, bf16, from a
     generator of its own (``make_grad``);
+  * shapes with shared K/V heads (``make_kv``): Q [B, H, N_q, d] then K and V
+    [B, H_kv, N_kv, d], standard normal, in that order;
   * a ``torch.Generator`` on the CPU, seeded with ``seed``;
   * Q, K, V drawn in that order in float32 with the distribution the workload
     names, then rounded to bf16 (round-to-nearest-even, torch's conversion);
@@ -27,7 +29,8 @@ from dataclasses import dataclass
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "workload", "make_inputs", "make_random", "make_grad", "sha256_of"]
+__all__ = ["Workload", "WORKLOADS", "workload", "make_inputs", "make_random", "make_grad", "KvWorkload",
+           "KV_WORKLOADS", "kv_workload", "make_kv", "sha256_of"]
 
 
 @dataclass(frozen=True)
@@ -126,6 +129,62 @@ def make_grad(B: int, H: int, N: int, d: int, seed: int) -> torch.Tensor:
     gen = torch.Generator(device="cpu")
     gen.manual_seed(int(seed) + 7919)
     return _draw(gen, (B, H, N, d), "normal")
+
+
+@dataclass(frozen=True)
+class KvWorkload:
+    """A shape with shared K/V heads: Q [B, H, N_q, d], K/V [B, H_kv, N_kv, d]."""
+    name: str
+    B: int
+    H: int
+    H_kv: int
+    N_q: int
+    N_kv: int
+    d: int
+    seed: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def kv_bytes(self) -> int:
+        """Bytes of K and V, read once by an exact kernel: the decode shape's traffic."""
+        return 2 * self.B * self.H_kv * self.N_kv * self.d * 2
+
+    @property
+    def flops(self) -> float:
+        return 4.0 * self.B * self.H * self.N_q * self.N_kv * self.d
+
+    def describe(self) -> dict:
+        return {"workload": self.name, "B": self.B, "H": self.H, "H_kv": self.H_kv, "N_q": self.N_q,
+                "N_kv": self.N_kv, "d": self.d, "q": "normal", "k": "normal", "v": "normal", "seed": self.seed,
+                "scale": "1/sqrt(d)", "causal": False}
+
+
+# Decode against a long K/V cache with grouped heads (32 query heads on 8 K/V
+# heads), one new token per sequence, batch 4.
+KV_WORKLOADS = [
+    KvWorkload("decode32k_gqa8_b4", 4, 32, 8, 1, 32768, 128, seed=2001),
+]
+
+
+def kv_workload(name: str) -> KvWorkload:
+    for w in KV_WORKLOADS:
+        if w.name == name:
+            return w
+    raise KeyError(name)
+
+
+def make_kv(B: int, H: int, H_kv: int, N_q: int, N_kv: int, d: int, seed: int):
+    """Q [B, H, N_q, d] and K, V [B, H_kv, N_kv, d], bf16, standard normal, drawn
+    in that order on the CPU from ``seed``."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(int(seed))
+    q = _draw(gen, (B, H, N_q, d), "normal")
+    k = _draw(gen, (B, H_kv, N_kv, d), "normal")
+    v = _draw(gen, (B, H_kv, N_kv, d), "normal")
+    return q, k, v
 
 
 def sha256_of(*tensors: torch.Tensor) -> str:

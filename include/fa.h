@@ -80,7 +80,8 @@ fa_status_t fa_fwd(const void* Q, const void* K, const void* V, void* O, float* 
  * wait since the last call, or FA_ERR_CUDA if the synchronisation failed.
  * `info`, if not NULL, receives 4 words describing the first timeout:
  * {role (forward: 1 producer, 2 mma, 3 softmax/epilogue; backward dQ kernel:
- * 4, 5, 6; backward dK/dV kernel: 7, 8, 9, in the same order), blockIdx.x, blockIdx.y,
+ * 4, 5, 6; backward dK/dV kernel: 7, 8, 9; short-query kernel of fa_fwd_kv:
+ * 10, 11, 12, in the same order), blockIdx.x, blockIdx.y,
  * blockIdx.z}; all zero when there was none.
  */
 fa_status_t fa_get_device_status(cudaStream_t stream, unsigned int* info);
@@ -139,6 +140,60 @@ fa_status_t fa_naive_fwd(const void* Q, const void* K, const void* V, void* O, f
  */
 fa_status_t fa_naive_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE,
                                  int B, int H, int N, int d, float scale, cudaStream_t stream);
+
+/*
+ * fa_fwd_kv -- the forward pass with shared key/value heads (GQA) and
+ * separate query and key lengths: the prefill and decode shapes of a model
+ * whose H query heads share H_kv key/value heads ("FlashAttention：IO 感知的
+ * 精确注意力", "与其他知识点的关系": grouped K/V heads combine with the exact,
+ * IO-aware kernel; "常见误区": decode is bandwidth-bound).
+ *   Q      : device, bf16 [B, H, N_q, d], read only.
+ *   K, V   : device, bf16 [B, H_kv, N_kv, d], read only. H must be a multiple
+ *            of H_kv; query head h attends to K/V head h / (H / H_kv).
+ *   O      : device, bf16 [B, H, N_q, d], written.
+ *   LSE    : device, float32 [B, H, N_q], written (natural log).
+ *   Every query row attends to all N_kv keys (no mask).
+ *   num_splits : N_q <= 128 only: the number of contiguous key ranges
+ *            computed by separate CTAs and merged with the online-softmax rule
+ *            ("Flash Attention (FA1)", derivation steps 4-5). 0 chooses one
+ *            wave of CTAs (fa_fwd_kv_num_splits); values above the number of
+ *            128-key blocks are capped. N_q > 128 takes the fused forward
+ *            kernel and needs num_splits <= 1.
+ *   workspace, workspace_bytes : device memory of at least
+ *            fa_fwd_kv_workspace_bytes(...) bytes, 128-byte aligned, not
+ *            overlapping any other buffer; may be NULL when that is 0 (one
+ *            split or N_q > 128).
+ * For N_q <= 128 the query rows of the heads sharing a K/V head are packed
+ * into one 128-row tile (min(H/H_kv, 128/N_q) heads per tile), so each K/V
+ * tile is read once per group. Launches: one kernel, plus one merge kernel
+ * when there is more than one split. Limits as for fa_fwd; FA_ERR_INVALID_ARG
+ * also when H is not a multiple of H_kv or for a missing, misaligned, small or
+ * overlapping workspace.
+ */
+fa_status_t fa_fwd_kv(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                      int B, int H, int H_kv, int N_q, int N_kv, int d, float scale,
+                      int num_splits, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* fa_fwd_kv_num_splits -- the split count fa_fwd_kv uses when num_splits is 0
+ * (1 when N_q > 128); 0 for invalid sizes. Depends on the current device's SM
+ * count. */
+int fa_fwd_kv_num_splits(int B, int H, int H_kv, int N_q, int N_kv, int d);
+
+/* fa_fwd_kv_workspace_bytes -- workspace bytes fa_fwd_kv needs for these sizes
+ * and num_splits (0 = the automatic choice): num_splits * B*H*N_q * (d + 1)
+ * float32 partial results when there is more than one split, else 0. */
+size_t fa_fwd_kv_workspace_bytes(int B, int H, int H_kv, int N_q, int N_kv, int d, int num_splits);
+
+/*
+ * fa_fwd_kv_fault_test -- TEST HOOK, not for production use. fa_fwd_kv with
+ * every device-side wait limited to `timeout_ns`, and, when drop_load >= 0 and
+ * N_q <= 128, the drop_load-th K/V tile load (K, V of a CTA's first block,
+ * then of its second, ...) skipped in every CTA; as for fa_fwd_fault_test.
+ */
+fa_status_t fa_fwd_kv_fault_test(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                                 int B, int H, int H_kv, int N_q, int N_kv, int d, float scale,
+                                 int num_splits, void* workspace, size_t workspace_bytes,
+                                 int drop_load, unsigned long long timeout_ns, cudaStream_t stream);
 
 /*
  * fa_bwd_workspace_bytes -- bytes of device workspace fa_bwd needs for

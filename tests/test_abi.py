@@ -168,3 +168,44 @@ def test_bwd_workspace_size(lib):
 ])
 def test_bwd_host_side_rejections(lib, kwargs, expect):
     assert bwd_call(lib, **kwargs) == expect
+
+
+def kv_call(lib, **kw):
+    args = dict(Q=A, K=A + GAP, V=A + 2 * GAP, O=A + 3 * GAP, L=A + 4 * GAP, B=1, H=8, Hkv=2, Nq=1, Nkv=4096, d=128,
+                scale=0.1, splits=4, ws=A + 5 * GAP, ws_bytes=1 << 40)
+    args.update(kw)
+    return lib.fa_fwd_kv(args["Q"], args["K"], args["V"], args["O"], args["L"], args["B"], args["H"], args["Hkv"],
+                         args["Nq"], args["Nkv"], args["d"], ctypes.c_float(args["scale"]), args["splits"], args["ws"],
+                         args["ws_bytes"], None)
+
+
+def test_kv_workspace_and_splits(lib):
+    # 4 splits of 8 query rows (H = 8, N_q = 1) with d = 128: 4 * 8 * 129 floats
+    assert fa.fa_fwd_kv_workspace_bytes(1, 8, 2, 1, 4096, 128, 4) == 4 * 8 * 129 * 4
+    assert fa.fa_fwd_kv_workspace_bytes(1, 8, 2, 1, 4096, 128, 1) == 0
+    assert fa.fa_fwd_kv_workspace_bytes(1, 8, 2, 1, 200, 128, 9) == 2 * 8 * 129 * 4   # capped at 2 key blocks
+    assert fa.fa_fwd_kv_workspace_bytes(1, 8, 2, 300, 300, 128, 0) == 0                # long queries: no split
+    assert fa.fa_fwd_kv_workspace_bytes(1, 8, 3, 1, 64, 128, 0) == 0                   # 8 % 3 != 0
+    assert fa.fa_fwd_kv_num_splits(1, 8, 2, 1, 200, 128) in (1, 2)
+    assert fa.fa_fwd_kv_num_splits(1, 8, 3, 1, 64, 128) == 0
+    assert fa.fa_fwd_kv_num_splits(1, 8, 2, 300, 300, 128) == 1
+
+
+@pytest.mark.parametrize("kwargs,expect", [
+    (dict(Hkv=3), fa.FA_ERR_INVALID_ARG),                        # H not a multiple of H_kv
+    (dict(Hkv=0), fa.FA_ERR_INVALID_ARG),
+    (dict(Nq=0), fa.FA_ERR_INVALID_ARG),
+    (dict(Nkv=0), fa.FA_ERR_INVALID_ARG),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(scale=-1.0), fa.FA_ERR_UNSUPPORTED),
+    (dict(ws=0), fa.FA_ERR_INVALID_ARG),                         # 4 splits need a workspace
+    (dict(ws=A + 5 * GAP + 16), fa.FA_ERR_INVALID_ARG),          # not 128-byte aligned
+    (dict(ws_bytes=4 * 8 * 129 * 4 - 1), fa.FA_ERR_INVALID_ARG),  # too small
+    (dict(ws=A + 2 * GAP), fa.FA_ERR_INVALID_ARG),               # overlaps V
+    (dict(O=A + GAP + 64), fa.FA_ERR_INVALID_ARG),               # O overlaps K
+    (dict(L=A + 3 * GAP + 4), fa.FA_ERR_INVALID_ARG),            # LSE overlaps O
+    (dict(Q=A + 8), fa.FA_ERR_INVALID_ARG),
+    (dict(Nq=300, Nkv=300, splits=2), fa.FA_ERR_UNSUPPORTED),    # no split for long query blocks
+])
+def test_kv_host_side_rejections(lib, kwargs, expect):
+    assert kv_call(lib, **kwargs) == expect

@@ -1,0 +1,137 @@
+"""Shared K/V heads and short query blocks (fa_fwd_kv) against the oracle, through
+the C ABI (needs a GB300).
+
+Reference: ``oracle.attention_gqa`` (query head h attends to K/V head
+h // (H / H_kv)); the "twice the baseline" rule compares with the bf16
+materialise-path reference evaluated on K/V repeated per query head.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_io_aware_34_gb300 import fa, inputs
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from exact_io_aware_34_gb300 import build
+    build.build()
+    fa.load_library()
+
+
+def run_kv(q, k, v, scale, num_splits=0):
+    o, lse = fa.fa_fwd_kv(q.cuda(), k.cuda(), v.cuda(), scale=scale, num_splits=num_splits)
+    torch.cuda.synchronize()
+    st, info = fa.fa_get_device_status()
+    assert st == fa.FA_OK, (fa.fa_status_string(st), info)
+    return o.cpu(), lse.cpu()
+
+
+def check_kv(q, k, v, scale, num_splits=0, two_x_rule=True):
+    o, lse = run_kv(q, k, v, scale, num_splits)
+    Q, K, V = (parity.to64(x) for x in (q, k, v))
+    O_ref, L_ref = oracle.attention_gqa(Q, K, V, scale)
+    err = parity.errors(o, lse, O_ref, L_ref)
+    assert err["finite"], err
+    assert err["o_max"] <= parity.TOL_O_MAX, err
+    assert err["o_fro"] <= parity.TOL_O_FRO, err
+    assert err["lse_max"] <= parity.TOL_LSE_MAX, err
+    if two_x_rule:
+        G = q.shape[1] // k.shape[1]
+        On = oracle.naive_bf16_attention(Q, np.repeat(K, G, axis=1), np.repeat(V, G, axis=1), scale)
+        err["naive_o_max"] = float(np.abs(On - O_ref).max())
+        assert err["o_max"] <= 2 * err["naive_o_max"], err
+    return err, o, lse
+
+
+# --- short query blocks (the packed, split-key kernel) ------------------------------
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N_q,G", [(1, 1), (1, 8), (3, 4), (16, 8), (64, 2), (128, 1), (100, 4)])
+@pytest.mark.parametrize("N_kv", [1, 100, 129, 1000])
+def test_short_queries(d, N_q, G, N_kv):
+    H_kv = 2
+    q, k, v = inputs.make_kv(2, G * H_kv, H_kv, N_q, N_kv, d, seed=N_q * 131 + G * 17 + N_kv + d)
+    err, _, _ = check_kv(q, k, v, 1 / math.sqrt(d), two_x_rule=N_kv >= 64)
+    print(d, N_q, G, N_kv, err)
+
+
+@pytest.mark.parametrize("num_splits", [1, 2, 3, 7, 64])
+def test_forced_splits(num_splits):
+    """Every split count gives the oracle's result (the merge of partial results)."""
+    q, k, v = inputs.make_kv(1, 16, 4, 5, 4000, 128, seed=300 + num_splits)
+    err, o, lse = check_kv(q, k, v, 1 / math.sqrt(128), num_splits=num_splits)
+    print(num_splits, fa.fa_fwd_kv_workspace_bytes(1, 16, 4, 5, 4000, 128, num_splits), err)
+
+
+def test_splits_agree_with_each_other():
+    q, k, v = inputs.make_kv(2, 8, 2, 1, 3000, 64, seed=310)
+    o1, l1 = run_kv(q, k, v, 0.125, num_splits=1)
+    o5, l5 = run_kv(q, k, v, 0.125, num_splits=5)
+    assert float((o1.float() - o5.float()).abs().max()) <= 1e-2
+    assert float((l1 - l5).abs().max()) <= 1e-4
+
+
+def test_spiky_keys_with_splits():
+    """Large logits and spiky keys, so the splits' maxima differ widely."""
+    q, k, v = inputs.make_kv(1, 8, 1, 4, 2048, 128, seed=320)
+    q = (q.float() * 3).to(torch.bfloat16)
+    k = (k.float() * 3).to(torch.bfloat16)
+    k[0, 0, 1500] = (k[0, 0, 1500].float() * 8).to(torch.bfloat16)
+    check_kv(q, k, v, 1 / math.sqrt(128), num_splits=6)
+
+
+# --- long query blocks with shared K/V heads (the fused forward kernel) -------------
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N_q,N_kv,G", [(300, 300, 4), (1000, 700, 2), (129, 2000, 8)])
+def test_long_queries(d, N_q, N_kv, G):
+    q, k, v = inputs.make_kv(1, 2 * G, 2, N_q, N_kv, d, seed=N_q + N_kv + G + d)
+    check_kv(q, k, v, 1 / math.sqrt(d))
+
+
+def test_kv_heads_equal_reduces_to_fa_fwd():
+    """H_kv = H and N_q = N_kv: the same result as fa_fwd, bit for bit."""
+    q, k, v = inputs.make_random(1, 4, 700, 128, seed=330)
+    o1, l1 = run_kv(q, k, v, 0.09)
+    o2, l2 = parity.run_gpu(q, k, v, 0.09)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1, l2)
+
+
+# --- the decode workload the bench times ---------------------------------------------
+def test_decode_workload_full():
+    w = inputs.kv_workload("decode32k_gqa8_b4")
+    q, k, v = inputs.make_kv(w.B, w.H, w.H_kv, w.N_q, w.N_kv, w.d, w.seed)
+    err, _, _ = check_kv(q, k, v, w.scale)
+    print(w.name, fa.fa_fwd_kv_num_splits(w.B, w.H, w.H_kv, w.N_q, w.N_kv, w.d), err)
+
+
+# --- failure path and rejections ---------------------------------------------------
+@pytest.mark.parametrize("drop", [0, 1, 4])
+def test_kv_dropped_load_times_out_cleanly(drop):
+    q, k, v = (x.cuda() for x in inputs.make_kv(1, 8, 2, 2, 2000, 128, seed=340 + drop))
+    o = torch.zeros_like(q)
+    lse = torch.zeros(1, 8, 2, device="cuda")
+    ws = torch.empty(fa.fa_fwd_kv_workspace_bytes(1, 8, 2, 2, 2000, 128, 3), dtype=torch.uint8, device="cuda")
+    st = fa.fa_fwd_kv_fault_test(q, k, v, o, lse, 0.1, 3, ws, drop, 20_000_000)
+    assert st == fa.FA_OK
+    st, info = fa.fa_get_device_status()
+    assert st == fa.FA_ERR_TIMEOUT, (st, info)
+    assert info[0] in (10, 11, 12)
+    assert fa.fa_get_device_status()[0] == fa.FA_OK
+    check_kv(q.cpu(), k.cpu(), v.cpu(), 0.1, num_splits=3)
+
+
+def test_kv_small_workspace_rejected():
+    q, k, v = (x.cuda() for x in inputs.make_kv(1, 8, 2, 1, 4000, 128, seed=350))
+    need = fa.fa_fwd_kv_workspace_bytes(1, 8, 2, 1, 4000, 128, 4)
+    ws = torch.empty(need - 128, dtype=torch.uint8, device="cuda")
+    with pytest.raises(fa.FaError):
+        fa.fa_fwd_kv(q, k, v, num_splits=4, workspace=ws)
