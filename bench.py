@@ -15,7 +15,10 @@ torchrun) every rank runs its own copy of the workload (independent problems,
 no collective on the data path): weak scaling.
 
 The same run also times the backward pass (fa_bwd, three launches) on the
-same workload and reports it under "bwd" (skip with --no-bwd).
+same workload and reports it under "bwd" (skip with --no-bwd), and a decode
+shape with shared K/V heads (fa_fwd_kv: B=4, 32 query heads on 8 K/V heads,
+one query row against 32768 keys, d=128) under "decode" in K/V GB/s against
+the HBM roofline (skip with --no-decode).
 
 --impl reference times the CPU oracle (float64, numpy) on the host cores, on a
 bounded sample of the same workload per step.
@@ -45,6 +48,9 @@ KERNEL_NAME = "fa_fwd_kernel<128>"
 KERNEL_SOURCES = ["exact_io_aware_34_gb300/csrc/fa_fwd_kernel.cuh", "exact_io_aware_34_gb300/csrc/sm103a_ptx.cuh"]
 BWD_KERNEL_SOURCES = ["exact_io_aware_34_gb300/csrc/fa_bwd_kernel.cuh", "exact_io_aware_34_gb300/csrc/fa_fwd_kernel.cuh",
                       "exact_io_aware_34_gb300/csrc/sm103a_ptx.cuh"]
+DECODE_KERNEL_SOURCES = ["exact_io_aware_34_gb300/csrc/fa_decode_kernel.cuh", "exact_io_aware_34_gb300/csrc/fa_fwd_kernel.cuh",
+                         "exact_io_aware_34_gb300/csrc/sm103a_ptx.cuh"]
+DECODE_WORKLOAD = "decode32k_gqa8_b4"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 
@@ -483,6 +489,49 @@ def run_native(args):
         del do, dq, dk, dv, ws_b
         torch.cuda.empty_cache()
 
+    # Decode with shared K/V heads (fa_fwd_kv, short-query kernel + merge):
+    # bandwidth-bound, so it is measured in K/V bytes per second against the
+    # HBM roofline. Same timing rules.
+    decode = None
+    if not args.no_decode:
+        dw = inputs.kv_workload(DECODE_WORKLOAD)
+        dq_, dk_, dv_ = (x.to(device) for x in inputs.make_kv(dw.B, dw.H, dw.H_kv, dw.N_q, dw.N_kv, dw.d, dw.seed))
+        splits = fa.fa_fwd_kv_num_splits(dw.B, dw.H, dw.H_kv, dw.N_q, dw.N_kv, dw.d)
+        dws_bytes = fa.fa_fwd_kv_workspace_bytes(dw.B, dw.H, dw.H_kv, dw.N_q, dw.N_kv, dw.d, 0)
+        dws = torch.empty(max(dws_bytes, 128), dtype=torch.uint8, device=device)
+        do_, dl_ = torch.empty_like(dq_), torch.empty(dq_.shape[:3], dtype=torch.float32, device=device)
+        for _ in range(args.warmup):
+            fa.fa_fwd_kv(dq_, dk_, dv_, do_, dl_, dw.scale, 0, dws)
+        torch.cuda.synchronize(device)
+        st, info = fa.fa_get_device_status()
+        if st != fa.FA_OK:
+            raise RuntimeError(f"device status after decode warm-up: {fa.fa_status_string(st)} {info}")
+        n_steps = max(3, min(args.steps, 50))
+        es = [torch.cuda.Event(enable_timing=True) for _ in range(n_steps)]
+        ee = [torch.cuda.Event(enable_timing=True) for _ in range(n_steps)]
+        with ClockSampler(local, uuid) as dclocks:
+            for i in range(n_steps):
+                flush.fill_(float(i))
+                es[i].record(stream)
+                fa.fa_fwd_kv(dq_, dk_, dv_, do_, dl_, dw.scale, 0, dws)
+                ee[i].record(stream)
+            torch.cuda.synchronize(device)
+        st, info = fa.fa_get_device_status()
+        if st != fa.FA_OK:
+            raise RuntimeError(f"device status after decode steps: {fa.fa_status_string(st)} {info}")
+        d_ms = [a.elapsed_time(b) for a, b in zip(es, ee)]
+        dec_ms = sum(d_ms) / n_steps
+        decode = {
+            "metric": "decode K/V read rate (GB/s: K and V bytes per call / time) with shared K/V heads",
+            "value": dw.kv_bytes / (dec_ms * 1e-3) / 1e9, "unit": "GB/s", "steps": n_steps, "ms_per_step": dec_ms,
+            "step_ms": {"min": min(d_ms), "median": statistics.median(d_ms), "max": max(d_ms)},
+            "tflops": dw.flops / (dec_ms * 1e-3) / 1e12, "config": dw.describe(), "num_splits": splits,
+            "kv_bytes_per_call": dw.kv_bytes, "workspace_bytes": dws_bytes,
+            "gpu_launches": n_steps * (2 if splits > 1 else 1), "clocks": dclocks.summary(),
+        }
+        del dq_, dk_, dv_, dws, do_, dl_
+        torch.cuda.empty_cache()
+
     # end to end through the public API: pinned host inputs in, O and LSE back out
     qh, kh, vh = (x.pin_memory() for x in (q, k, v))
     oh = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
@@ -541,6 +590,13 @@ def run_native(args):
                                "peak_source": f"{peak_src} dense bf16 burst",
                                "kernels": "bwd_prep_kernel, fa_bwd_dq_kernel<%d>, fa_bwd_dkdv_kernel<%d>" % (d, d)}
             line["bwd"] = bwd
+        if decode is not None:
+            decode["roofline"] = {"bound": "hbm", "achieved": decode["value"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                  "frac": decode["value"] / peaks["hbm_gbs"],
+                                  "traffic": load_traffic(DECODE_WORKLOAD, "", DECODE_KERNEL_SOURCES),
+                                  "peak_source": f"{peak_src} HBM copy bandwidth",
+                                  "kernels": "fa_decode_kernel<%d> + decode_merge_kernel<%d>" % (d, d)}
+            line["decode"] = decode
         if cpu is not None:
             line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)
@@ -562,6 +618,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-comparator", action="store_true", help="skip timing standard attention (S/P in HBM)")
     ap.add_argument("--no-bwd", action="store_true", help="skip timing the backward pass")
+    ap.add_argument("--no-decode", action="store_true", help="skip timing the shared-K/V-head decode shape")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

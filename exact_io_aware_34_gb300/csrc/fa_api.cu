@@ -441,7 +441,7 @@ int device_sm_count() {
 }
 
 // Packing and key split of the short-query path (N_q <= 128). With
-// num_splits <= 0 the split count fills one wave of CTAs (one per SM); it
+// num_splits <= 0 the split count fills one wave of CTAs (two per SM); it
 // is capped by the number of key blocks, and ranges are whole blocks with
 // no empty range.
 KvPlan kv_plan(int B, int H, int H_kv, int N_q, int N_kv, int num_splits) {
@@ -454,7 +454,8 @@ KvPlan kv_plan(int B, int H, int H_kv, int N_q, int N_kv, int num_splits) {
   if (s <= 0) {
     const long long base = static_cast<long long>(B) * H_kv * k.tiles_per_group;
     const int sms = device_sm_count();
-    s = base >= sms ? 1 : static_cast<int>(sms / base);
+    const long long slots = static_cast<long long>(sms) * 2;   // resident short-query CTAs (two per SM)
+    s = base >= slots ? 1 : static_cast<int>(slots / base);
   }
   s = std::max(1, std::min(s, k.n_kv_blocks));
   k.blocks_per_split = (k.n_kv_blocks + s - 1) / s;

@@ -26,7 +26,10 @@
 // tile (one thread per row), warp 4 is the TMA producer, warp 5 allocates
 // TMEM and issues the MMAs. TMEM: S at column 0 (P, packed bf16, over its
 // first 64 columns), O at column 128. The per-block update is the forward
-// kernel's, including the lazy rescale.
+// kernel's, including the lazy rescale. With a single tile, a CTA's QK^T,
+// softmax and PV of a block run one after another; two CTAs per SM (a
+// 2-slot K/V ring each) overlap one CTA's softmax with the other's loads and
+// MMAs.
 #pragma once
 
 #include "fa_fwd_kernel.cuh"
@@ -42,7 +45,8 @@ struct DecCfg {
   static constexpr int kChunks = HD / 64;
   static constexpr int kChunkBytes = 128 * 128;
   static constexpr int kTileBytes = kChunks * kChunkBytes;
-  static constexpr int kStages = (HD == 128) ? 6 : 12;     // K/V ring slots
+  static constexpr int kStages = (HD == 128) ? 2 : 4;      // K/V ring slots
+  static constexpr int kCtasPerSm = 2;                       // 2 x (Q + ring) fits shared memory, 2 x 256 TMEM
   static constexpr int kSmemBytes = kTileBytes + kStages * kTileBytes + 1024;
   static constexpr int kThreads = 192;
   static constexpr uint32_t kTmemCols = 256;
@@ -73,7 +77,7 @@ struct DecParams {
 };
 
 template <int HD>
-__global__ void __launch_bounds__(DecCfg<HD>::kThreads, 1)
+__global__ void __launch_bounds__(DecCfg<HD>::kThreads, DecCfg<HD>::kCtasPerSm)
     fa_decode_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const DecParams p) {
   using C = DecCfg<HD>;
