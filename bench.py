@@ -235,12 +235,45 @@ _INPUT_CACHE = {}
 
 
 def _cached_inputs(name):
-    """The workload's inputs as float32 numpy arrays, generated once per process."""
+    """The workload's inputs as float32 numpy arrays, generated once per process.
+    ``bwd:<name>`` adds the backward's dO; ``kv:<name>`` is a shared-K/V-head shape."""
     from exact_io_aware_34_gb300 import inputs as _inp
     if name not in _INPUT_CACHE:
-        q, k, v, s = _inp.make_inputs(_inp.workload(name))
-        _INPUT_CACHE[name] = (q.float().numpy(), k.float().numpy(), v.float().numpy(), s)
+        if name.startswith("kv:"):
+            w = _inp.kv_workload(name[3:])
+            q, k, v = _inp.make_kv(w.B, w.H, w.H_kv, w.N_q, w.N_kv, w.d, w.seed)
+            _INPUT_CACHE[name] = (q.float().numpy(), k.float().numpy(), v.float().numpy(), w.scale)
+        elif name.startswith("bwd:"):
+            w = _inp.workload(name[4:])
+            q, k, v, s = _inp.make_inputs(w)
+            do = _inp.make_grad(w.B, w.H, w.N, w.d, w.seed)
+            _INPUT_CACHE[name] = (q.float().numpy(), k.float().numpy(), v.float().numpy(), do.float().numpy(), s)
+        else:
+            q, k, v, s = _inp.make_inputs(_inp.workload(name))
+            _INPUT_CACHE[name] = (q.float().numpy(), k.float().numpy(), v.float().numpy(), s)
     return _INPUT_CACHE[name]
+
+
+def _oracle_bwd_worker(args):
+    """Pool task: the backward oracle's work for query-row chunks (b, h, r0, r1):
+    dQ of those rows and their contributions to dK and dV. Returns seconds."""
+    import oracle as _oracle
+    name, chunks = args
+    Q, K, V, dO, s = _cached_inputs(name)
+    t0 = time.perf_counter()
+    for b, h, r0, r1 in chunks:
+        _oracle.attention_bwd_heads(Q[:, :, r0:r1], K, V, dO[:, :, r0:r1], s, [(b, h)])
+    return time.perf_counter() - t0
+
+
+def _oracle_kv_worker(args):
+    """Pool task: the shared-K/V-head oracle on the given (b, h) query heads. Returns seconds."""
+    import oracle as _oracle
+    name, heads = args
+    Q, K, V, s = _cached_inputs(name)
+    t0 = time.perf_counter()
+    _oracle.attention_gqa_rows(Q, K, V, s, heads)
+    return time.perf_counter() - t0
 
 
 def _worker_init(name, ready):
@@ -257,17 +290,17 @@ class OracleTimer:
     single-threaded worker processes (one per host core). Every worker builds
     its copy of the inputs before the first timed task."""
 
-    def __init__(self, name: str, cores: int | None = None):
+    def __init__(self, name: str, cores: int | None = None, init_name: str | None = None):
         import multiprocessing as mp
         from exact_io_aware_34_gb300 import inputs as _inp
         self.name = name
-        self.w = _inp.workload(name)
+        self.w = _inp.workload(name) if not name.startswith("kv:") else None
         self.cores = cores or len(os.sched_getaffinity(0))
         os.environ["OPENBLAS_NUM_THREADS"] = "1"
         os.environ["OMP_NUM_THREADS"] = "1"
         ctx = mp.get_context("spawn")
         ready = ctx.Barrier(self.cores)
-        self.pool = ctx.Pool(self.cores, initializer=_worker_init, initargs=(name, ready))
+        self.pool = ctx.Pool(self.cores, initializer=_worker_init, initargs=(init_name or name, ready))
         self.pool.map(_noop, range(4 * self.cores), chunksize=1)
 
     def run(self, n_rows: int, seed: int = 0):
@@ -301,6 +334,58 @@ class OracleTimer:
     def close(self):
         self.pool.terminate()
         self.pool.join()
+
+
+def cpu_baseline_bwd(name: str, target_s: float = 10.0):
+    """The backward oracle (float64 numpy) on query-row chunks sampled from the
+    workload, one single-threaded process per host core; TFLOP/s counting the
+    five N x N x d products (10 * rows * N * d per chunk)."""
+    import numpy as np
+    from exact_io_aware_34_gb300 import inputs as _inp
+    w = _inp.workload(name)
+    t = OracleTimer(name, init_name="bwd:" + name)
+    try:
+        rng = np.random.default_rng(3)
+        rows_per_chunk = 64
+        n_chunks = t.cores
+        while True:
+            heads = rng.integers(0, w.B * w.H, size=n_chunks)
+            starts = rng.integers(0, w.N - rows_per_chunk + 1, size=n_chunks)
+            chunks = [(int(x // w.H), int(x % w.H), int(r0), int(r0) + rows_per_chunk) for x, r0 in zip(heads, starts)]
+            parts = [c.tolist() for c in np.array_split(np.array(chunks), t.cores) if len(c)]
+            t0 = time.perf_counter()
+            t.pool.map(_oracle_bwd_worker, [("bwd:" + name, [tuple(x) for x in p]) for p in parts])
+            dt = time.perf_counter() - t0
+            if dt >= 0.5 * target_s or n_chunks >= 1024 * t.cores:
+                break
+            n_chunks = min(1024 * t.cores, max(n_chunks * 2, int(n_chunks * target_s / max(dt, 1e-3))))
+    finally:
+        t.close()
+    flops = 10.0 * n_chunks * rows_per_chunk * w.N * w.d
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": t.cores, "kind": "oracle",
+            "sample": f"{n_chunks} chunks of {rows_per_chunk} query rows of the {name} workload (dQ rows and their "
+                      f"dK, dV contributions over all {w.N} keys), float64 numpy backward oracle, {t.cores} "
+                      f"single-threaded worker processes, {dt:.1f} s"}
+
+
+def cpu_baseline_decode(name: str):
+    """The shared-K/V-head oracle over every query head of the decode workload,
+    one single-threaded process per host core; GB/s of K/V processed."""
+    import numpy as np
+    from exact_io_aware_34_gb300 import inputs as _inp
+    w = _inp.kv_workload(name)
+    t = OracleTimer("kv:" + name)
+    try:
+        heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+        parts = [[tuple(int(v) for v in x) for x in c] for c in np.array_split(np.array(heads), t.cores) if len(c)]
+        t0 = time.perf_counter()
+        t.pool.map(_oracle_kv_worker, [("kv:" + name, p) for p in parts])
+        dt = time.perf_counter() - t0
+    finally:
+        t.close()
+    return {"value": w.kv_bytes / dt / 1e9, "unit": "GB/s", "cores": t.cores, "kind": "oracle",
+            "sample": f"the whole {name} workload ({len(heads)} query heads, {w.N_kv} keys each), float64 numpy "
+                      f"oracle, {t.cores} single-threaded worker processes, {dt:.2f} s"}
 
 
 def cpu_baseline(name: str, target_s: float = 15.0):
@@ -363,9 +448,13 @@ def run_native(args):
     torch.cuda.set_device(device)
 
     # The CPU baseline runs before the first GPU call (its worker pool is spawned).
-    cpu = None
+    cpu = cpu_bwd = cpu_dec = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.workload, target_s=args.cpu_seconds)
+        if not args.no_bwd:
+            cpu_bwd = cpu_baseline_bwd(args.workload, target_s=min(10.0, args.cpu_seconds))
+        if not args.no_decode:
+            cpu_dec = cpu_baseline_decode(DECODE_WORKLOAD)
 
     from exact_io_aware_34_gb300 import build as fa_build
     from exact_io_aware_34_gb300 import fa, inputs
@@ -589,6 +678,8 @@ def run_native(args):
                                "traffic": load_traffic(w.name, ":bwd", BWD_KERNEL_SOURCES),
                                "peak_source": f"{peak_src} dense bf16 burst",
                                "kernels": "bwd_prep_kernel, fa_bwd_dq_kernel<%d>, fa_bwd_dkdv_kernel<%d>" % (d, d)}
+            if cpu_bwd is not None:
+                bwd["cpu_baseline"] = cpu_bwd
             line["bwd"] = bwd
         if decode is not None:
             decode["roofline"] = {"bound": "hbm", "achieved": decode["value"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -596,6 +687,8 @@ def run_native(args):
                                   "traffic": load_traffic(DECODE_WORKLOAD, "", DECODE_KERNEL_SOURCES),
                                   "peak_source": f"{peak_src} HBM copy bandwidth",
                                   "kernels": "fa_decode_kernel<%d> + decode_merge_kernel<%d>" % (d, d)}
+            if cpu_dec is not None:
+                decode["cpu_baseline"] = cpu_dec
             line["decode"] = decode
         if cpu is not None:
             line["cpu_baseline"] = cpu

@@ -83,3 +83,12 @@ def test_clock_summary_nvml_samples():
     s = c.summary()
     assert s["sm_mhz"] == 1950.0 and s["sm_max_mhz"] == 2070.0 and s["source"] == "nvml"
     assert s["reasons"] == ["hw_slowdown", "sw_power_cap"] and s["samples"] == 3
+
+
+def test_cpu_baselines_of_the_next_rows():
+    """The backward and decode oracle timings return well-formed records (tiny samples)."""
+    import bench
+    rb = bench.cpu_baseline_bwd("n256_d64", target_s=0.5)
+    assert rb["kind"] == "oracle" and rb["unit"] == "TFLOP/s" and rb["value"] > 0 and rb["cores"] >= 1
+    rd = bench.cpu_baseline_decode("decode32k_gqa8_b4")
+    assert rd["kind"] == "oracle" and rd["unit"] == "GB/s" and rd["value"] > 0
