@@ -378,14 +378,20 @@ def cpu_baseline_decode(name: str):
     try:
         heads = [(b, h) for b in range(w.B) for h in range(w.H)]
         parts = [[tuple(int(v) for v in x) for x in c] for c in np.array_split(np.array(heads), t.cores) if len(c)]
+        # the whole workload, repeated until about 3 s of wall time have passed
+        reps = 0
         t0 = time.perf_counter()
-        t.pool.map(_oracle_kv_worker, [("kv:" + name, p) for p in parts])
-        dt = time.perf_counter() - t0
+        while True:
+            t.pool.map(_oracle_kv_worker, [("kv:" + name, p) for p in parts])
+            reps += 1
+            dt = time.perf_counter() - t0
+            if dt >= 3.0 or reps >= 1000:
+                break
     finally:
         t.close()
-    return {"value": w.kv_bytes / dt / 1e9, "unit": "GB/s", "cores": t.cores, "kind": "oracle",
-            "sample": f"the whole {name} workload ({len(heads)} query heads, {w.N_kv} keys each), float64 numpy "
-                      f"oracle, {t.cores} single-threaded worker processes, {dt:.2f} s"}
+    return {"value": reps * w.kv_bytes / dt / 1e9, "unit": "GB/s", "cores": t.cores, "kind": "oracle",
+            "sample": f"the whole {name} workload ({len(heads)} query heads, {w.N_kv} keys each) {reps} times, "
+                      f"float64 numpy oracle, {t.cores} single-threaded worker processes, {dt:.2f} s"}
 
 
 def cpu_baseline(name: str, target_s: float = 15.0):
