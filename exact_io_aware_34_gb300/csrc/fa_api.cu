@@ -622,6 +622,33 @@ fa_status_t fa_fwd_kv_fault_test(const void* Q, const void* K, const void* V, vo
                  drop_load < 0 ? -1 : drop_load, timeout_ns, stream);
 }
 
+fa_status_t fa_merge_partials(const float* O_parts, const float* LSE_parts, void* O, float* LSE, int num_parts,
+                              long long rows, int d, cudaStream_t stream) {
+  if (!O_parts || !LSE_parts || !O || !LSE || num_parts < 1 || rows < 1) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (rows >= (1LL << 31) / 8) return FA_ERR_INVALID_ARG;
+  const void* ptrs[4] = {O_parts, LSE_parts, O, LSE};
+  for (const void* ptr : ptrs)
+    if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return FA_ERR_INVALID_ARG;
+  const size_t n_op = static_cast<size_t>(num_parts) * rows * d * 4;
+  const size_t n_lp = static_cast<size_t>(num_parts) * rows * 4;
+  const size_t n_o = static_cast<size_t>(rows) * d * 2;
+  const size_t n_l = static_cast<size_t>(rows) * 4;
+  if (overlaps(O, n_o, O_parts, n_op) || overlaps(O, n_o, LSE_parts, n_lp) || overlaps(LSE, n_l, O_parts, n_op) ||
+      overlaps(LSE, n_l, LSE_parts, n_lp) || overlaps(O, n_o, LSE, n_l))
+    return FA_ERR_INVALID_ARG;
+  const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
+  if (d == 64)
+    fa::decode_merge_kernel<64><<<grid, 256, 0, stream>>>(O_parts, LSE_parts, static_cast<__nv_bfloat16*>(O), LSE,
+                                                         rows, num_parts);
+  else
+    fa::decode_merge_kernel<128><<<grid, 256, 0, stream>>>(O_parts, LSE_parts, static_cast<__nv_bfloat16*>(O), LSE,
+                                                          rows, num_parts);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FA_OK;
+}
+
 fa_status_t fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
                    void* dQ, void* dK, void* dV, int B, int H, int N, int d, float scale, void* workspace,
                    size_t workspace_bytes, cudaStream_t stream) {

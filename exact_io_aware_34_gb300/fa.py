@@ -27,7 +27,7 @@ FA_ERR_TIMEOUT = 4
 EXPORTED = ("fa_fwd", "fa_get_device_status", "fa_status_string", "fa_last_cuda_error", "fa_fwd_fault_test",
             "fa_naive_fwd", "fa_naive_workspace_bytes", "fa_naive_fwd_noalloc", "fa_bwd", "fa_bwd_workspace_bytes",
             "fa_bwd_fault_test", "fa_fwd_kv", "fa_fwd_kv_num_splits", "fa_fwd_kv_workspace_bytes",
-            "fa_fwd_kv_fault_test")
+            "fa_fwd_kv_fault_test", "fa_merge_partials")
 
 _lib = None
 
@@ -81,6 +81,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_fwd_kv_num_splits.restype = i
     lib.fa_fwd_kv_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
     lib.fa_fwd_kv_workspace_bytes.restype = ctypes.c_size_t
+    lib.fa_merge_partials.argtypes = [vp, vp, vp, vp, i, ctypes.c_longlong, i, vp]
+    lib.fa_merge_partials.restype = i
     _lib = lib
     return lib
 
@@ -242,6 +244,33 @@ def fa_fwd_kv_fault_test(q, k, v, o, lse, scale: float, num_splits: int, workspa
             d, float(scale), int(num_splits), workspace.data_ptr() if workspace is not None else None,
             workspace.numel() * workspace.element_size() if workspace is not None else 0, int(drop_load),
             int(timeout_ns), _stream_handle(stream, q.device)))
+
+
+def fa_merge_partials(o_parts: torch.Tensor, lse_parts: torch.Tensor, o=None, lse=None, stream=None):
+    """Merge partial results over disjoint key sets (see include/fa.h).
+
+    o_parts: float32 CUDA [P, ..., d]; lse_parts: float32 CUDA [P, ...] with the
+    same leading shape. Returns (o bf16 [..., d], lse float32 [...]).
+    """
+    for name, t in (("o_parts", o_parts), ("lse_parts", lse_parts)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous float32 CUDA tensor")
+    if o_parts.shape[:-1] != lse_parts.shape or o_parts.dim() < 3:
+        raise ValueError(f"shapes do not match: {tuple(o_parts.shape)} vs {tuple(lse_parts.shape)}")
+    P, d = o_parts.shape[0], o_parts.shape[-1]
+    out_shape = tuple(o_parts.shape[1:])
+    rows = int(lse_parts[0].numel())
+    if o is None:
+        o = torch.empty(out_shape, dtype=torch.bfloat16, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty(out_shape[:-1], dtype=torch.float32, device=o_parts.device)
+    lib = load_library()
+    with torch.cuda.device(o_parts.device):
+        st = lib.fa_merge_partials(o_parts.data_ptr(), lse_parts.data_ptr(), o.data_ptr(), lse.data_ptr(), int(P), rows,
+                                   int(d), _stream_handle(stream, o_parts.device))
+    if st != FA_OK:
+        raise FaError(st, "fa_merge_partials")
+    return o, lse
 
 
 def fa_bwd_workspace_bytes(B: int, H: int, N: int) -> int:

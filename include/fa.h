@@ -196,6 +196,24 @@ fa_status_t fa_fwd_kv_fault_test(const void* Q, const void* K, const void* V, vo
                                  int drop_load, unsigned long long timeout_ns, cudaStream_t stream);
 
 /*
+ * fa_merge_partials -- combine attention results computed over disjoint key
+ * sets into the result over their union, by the online-softmax rule
+ * ("Flash Attention (FA1)", derivation steps 4-5, in log-sum-exp form):
+ *     LSE = ln sum_p e^{LSE_p},   O = sum_p e^{LSE_p - LSE} O_p.
+ * This is the exchange step of a sequence split of K/V across devices: each
+ * device computes (O_p, LSE_p) for its key shard (fa_fwd / fa_fwd_kv), the
+ * partial results are gathered, and one call merges them.
+ *   O_parts   : device, float32 [num_parts][rows][d], each normalised by its own l_p.
+ *   LSE_parts : device, float32 [num_parts][rows], natural log.
+ *   O         : device, bf16 [rows][d], written.   LSE : device, float32 [rows], written.
+ *   rows      : number of query rows (e.g. B*H*N_q); d in {64, 128}.
+ * All pointers 16-byte aligned; outputs must not overlap inputs or each other.
+ * One kernel launch on `stream`.
+ */
+fa_status_t fa_merge_partials(const float* O_parts, const float* LSE_parts, void* O, float* LSE,
+                              int num_parts, long long rows, int d, cudaStream_t stream);
+
+/*
  * fa_bwd_workspace_bytes -- bytes of device workspace fa_bwd needs for
  * B x H heads of length N: two float32 values per query row, rows padded to
  * a multiple of 128. Returns 0 for non-positive sizes.

@@ -209,3 +209,19 @@ def test_kv_workspace_and_splits(lib):
 ])
 def test_kv_host_side_rejections(lib, kwargs, expect):
     assert kv_call(lib, **kwargs) == expect
+
+
+@pytest.mark.parametrize("kwargs,expect", [
+    (dict(Op=0), fa.FA_ERR_INVALID_ARG),
+    (dict(P=0), fa.FA_ERR_INVALID_ARG),
+    (dict(rows=0), fa.FA_ERR_INVALID_ARG),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(O=A + 8), fa.FA_ERR_INVALID_ARG),                  # misaligned
+    (dict(O=A + 256), fa.FA_ERR_INVALID_ARG),                # O overlaps the partial O
+    (dict(L=A + 3 * GAP + 64), fa.FA_ERR_INVALID_ARG),       # LSE overlaps O
+])
+def test_merge_host_side_rejections(lib, kwargs, expect):
+    args = dict(Op=A, Lp=A + GAP, O=A + 3 * GAP, L=A + 3 * GAP + (1 << 20), P=4, rows=1000, d=128)
+    args.update(kwargs)
+    assert lib.fa_merge_partials(args["Op"], args["Lp"], args["O"], args["L"], args["P"], args["rows"], args["d"],
+                                 None) == expect

@@ -135,3 +135,37 @@ def test_kv_small_workspace_rejected():
     ws = torch.empty(need - 128, dtype=torch.uint8, device="cuda")
     with pytest.raises(fa.FaError):
         fa.fa_fwd_kv(q, k, v, num_splits=4, workspace=ws)
+
+
+# --- merging partial results (the exchange step of a sequence split) ----------------
+def test_merge_partials_matches_oracle():
+    rng = np.random.default_rng(360)
+    P, rows, d = 5, 300, 128
+    o_parts = torch.from_numpy(rng.standard_normal((P, 3, rows // 3, d)).astype(np.float32))
+    lse_parts = torch.from_numpy((rng.standard_normal((P, 3, rows // 3)) * 20).astype(np.float32))
+    o, lse = fa.fa_merge_partials(o_parts.cuda(), lse_parts.cuda())
+    torch.cuda.synchronize()
+    O_ref, L_ref = oracle.merge_partials(o_parts.double().numpy(), lse_parts.double().numpy())
+    assert float(np.abs(o.float().cpu().numpy() - O_ref).max()) <= 2 ** -8 * float(np.abs(O_ref).max()) + 1e-6
+    assert float(np.abs(lse.cpu().numpy() - L_ref).max()) <= 1e-4
+
+
+@pytest.mark.parametrize("world", [2, 3, 8])
+def test_sequence_split_emulated_on_one_gpu(world):
+    """The ranks of a sequence split, run one after another on one GPU: each
+    shard's partial result from fa_fwd_kv, then one fa_merge_partials call,
+    against the oracle over all keys."""
+    from exact_io_aware_34_gb300 import cp
+    q, k, v = inputs.make_kv(1, 8, 2, 300, 5000, 128, seed=370 + world)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    parts = []
+    for r in range(world):
+        s0, s1 = cp.shard_bounds(5000, world, r)
+        parts.append(fa.fa_fwd_kv(qd, kd[:, :, s0:s1].contiguous(), vd[:, :, s0:s1].contiguous(), scale=0.09))
+    o, lse = fa.fa_merge_partials(torch.stack([p[0].float() for p in parts]), torch.stack([p[1] for p in parts]))
+    torch.cuda.synchronize()
+    O_ref, L_ref = oracle.attention_gqa(parity.to64(q), parity.to64(k), parity.to64(v), 0.09)
+    err = parity.errors(o.cpu(), lse.cpu(), O_ref, L_ref)
+    assert err["finite"] and err["o_max"] <= parity.TOL_O_MAX and err["o_fro"] <= parity.TOL_O_FRO, err
+    assert err["lse_max"] <= parity.TOL_LSE_MAX, err
+    print(world, err)
