@@ -179,14 +179,16 @@ fa_status_t naive_launch(const void* Q, const void* K, const void* V, void* O, f
   std::call_once(once[dev], [&] {
     attr_err[dev] = gemm_attr<128, true>();
     if (attr_err[dev] == cudaSuccess) attr_err[dev] = gemm_attr<HD, false>();
+
   });
   if (attr_err[dev] != cudaSuccess) return cuda_fail(attr_err[dev]);
 
   const int BH = B * H;
   const long long ld = naive_ld(N);
-  CUtensorMap mq, mk, mp, mv;
+  CUtensorMap mq, mk, mp, mv, ms_out, mo_out;
   if (!make_map_ld(&mq, Q, BH, N, HD, HD, 64, 128) || !make_map_ld(&mk, K, BH, N, HD, HD, 64, 128) ||
-      !make_map_ld(&mp, ws, BH, N, N, ld, 64, 128) || !make_map_ld(&mv, V, BH, N, HD, HD, 64, 64))
+      !make_map_ld(&mp, ws, BH, N, N, ld, 64, 128) || !make_map_ld(&mv, V, BH, N, HD, HD, 64, 64) ||
+      !make_map_ld(&ms_out, ws, BH, N, N, ld, 64, 32) || !make_map_ld(&mo_out, O, BH, N, HD, HD, 64, 32))
     return cuda_fail(cudaErrorInvalidValue);
   auto* S = static_cast<__nv_bfloat16*>(ws);
 
@@ -194,19 +196,20 @@ fa_status_t naive_launch(const void* Q, const void* K, const void* V, void* O, f
   fa::naive::GemmParams g1{S, N, N, HD, static_cast<int>(ld), scale, kNaiveTimeoutNs};
   using G1 = fa::naive::GemmCfg<128, true>;
   fa::naive::gemm_bf16_kernel<128, true><<<dim3((N + 127) / 128, (N + 127) / 128, BH), G1::kThreads, G1::kSmemBytes,
-                                           stream>>>(mq, mk, g1);
+                                           stream>>>(mq, mk, ms_out, g1);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   // 2. P = softmax(S) row by row, in place; LSE = m + ln l
-  fa::naive::softmax_rows_kernel<<<static_cast<unsigned>(static_cast<long long>(BH) * N), 256, 0, stream>>>(
-      S, LSE, N, static_cast<int>(ld));
+  const long long n_rows = static_cast<long long>(BH) * N;
+  fa::naive::softmax_rows_kernel<<<static_cast<unsigned>((n_rows + 7) / 8), 256, 0, stream>>>(
+      S, LSE, n_rows, N, static_cast<int>(ld));
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   // 3. O = bf16(P V)
   fa::naive::GemmParams g2{static_cast<__nv_bfloat16*>(O), N, HD, N, HD, 1.0f, kNaiveTimeoutNs};
   using G2 = fa::naive::GemmCfg<HD, false>;
   fa::naive::gemm_bf16_kernel<HD, false><<<dim3(1, (N + 127) / 128, BH), G2::kThreads, G2::kSmemBytes, stream>>>(
-      mp, mv, g2);
+      mp, mv, mo_out, g2);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   return FA_OK;

@@ -13,8 +13,11 @@
 // with A row-major [M][K] (K-major operand) and B either [Nc][K] (K-major,
 // for S = Q K^T) or [K][Nc] (MN-major, for O = P V). One CTA computes a
 // 128 x BN tile of C; warp 4 loads A and B chunks of 64 k with TMA into a
-// ring, warp 5 issues the tcgen05 MMAs into TMEM, warps 0-3 convert and
-// store the accumulator (one row per thread).
+// ring, warp 5 issues the tcgen05 MMAs into TMEM, warps 0-3 convert the
+// accumulator (one row per thread), stage it in shared memory in the
+// 128-byte swizzled layout and write it with TMA stores (each warp its own
+// 32 rows). The S = Q K^T instance (K = d, two ring steps per tile) keeps a
+// 2-slot ring so that three CTAs share an SM and overlap their epilogues.
 #pragma once
 
 #include <cuda.h>
@@ -33,7 +36,8 @@ struct GemmCfg {
   static constexpr int kABytes = kBM * kBK * 2;           // 16 KB
   static constexpr int kBBytes = BN * kBK * 2;            // BN x 64 bf16
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = 4;
+  static constexpr int kStages = B_KMAJOR ? 2 : 4;
+  static constexpr int kCtasPerSm = B_KMAJOR ? 3 : 1;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
   static constexpr int kThreads = 192;                    // 6 warps
   static constexpr uint32_t kTmemCols = BN < 32 ? 32 : BN;
@@ -78,9 +82,9 @@ __device__ __forceinline__ bool naive_wait_warp(uint32_t bar, uint32_t parity, v
 }
 
 template <int BN, bool B_KMAJOR>
-__global__ void __launch_bounds__(GemmCfg<BN, B_KMAJOR>::kThreads, 1)
+__global__ void __launch_bounds__(GemmCfg<BN, B_KMAJOR>::kThreads, GemmCfg<BN, B_KMAJOR>::kCtasPerSm)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const GemmParams p) {
+                     const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
   using C = GemmCfg<BN, B_KMAJOR>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full[C::kStages];
@@ -176,41 +180,48 @@ __global__ void __launch_bounds__(GemmCfg<BN, B_KMAJOR>::kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------ epilogue: one row per thread
+    // ------------------------------------------------ epilogue: TMEM -> swizzled SMEM -> TMA store
     if (naive_wait_warp(ptx::smem_u32(&bar_acc), 0, abort_ptr, p.timeout_ns, 3)) {
       ptx::tc_fence_after();
       const int row = warp * 32 + lane;
-      const int m = m0 + row;
       const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-      __nv_bfloat16* crow = p.C + (static_cast<size_t>(z) * p.M + m) * p.ldc + n0;
-      const bool full_row = n0 + BN <= p.Nc;
+      // The ring is idle once the accumulator is complete: stage the tile at
+      // its start as BN/64 chunks of 128 rows x 128 bytes.
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t acc[32];
         ptx::tmem_ld32(taddr + 32 * c, acc);
         ptx::tmem_ld_wait();
         ptx::reg_fence32(acc);
-        if (m < p.M) {
-          uint32_t packed[16];
+        uint32_t packed[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            // round the fp32 sum to bf16, then apply alpha and round again
-            const float a0 = __bfloat162float(__float2bfloat16_rn(__uint_as_float(acc[2 * i]))) * p.alpha;
-            const float a1 = __bfloat162float(__float2bfloat16_rn(__uint_as_float(acc[2 * i + 1]))) * p.alpha;
-            packed[i] = ptx::pack_bf16x2(a0, a1);
-          }
-          if (full_row) {
-            uint4* dst = reinterpret_cast<uint4*>(crow + 32 * c);
+        for (int i = 0; i < 16; ++i) {
+          // round the fp32 sum to bf16, then apply alpha and round again
+          const float a0 = __bfloat162float(__float2bfloat16_rn(__uint_as_float(acc[2 * i]))) * p.alpha;
+          const float a1 = __bfloat162float(__float2bfloat16_rn(__uint_as_float(acc[2 * i + 1]))) * p.alpha;
+          packed[i] = ptx::pack_bf16x2(a0, a1);
+        }
+        const uint32_t row_addr = base + (c >> 1) * (C::kBM * 128) + row * 128;
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
-          } else {
-            const __nv_bfloat16* vals = reinterpret_cast<const __nv_bfloat16*>(packed);
-            for (int i = 0; i < 32; ++i)
-              if (n0 + 32 * c + i < p.Nc) crow[32 * c + i] = vals[i];
-          }
+        for (int v = 0; v < 4; ++v) {
+          const uint32_t unit = 4 * (c & 1) + v;       // 16-byte unit within the 128-byte row
+          const uint32_t addr = row_addr + ((unit ^ static_cast<uint32_t>(row & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(packed[4 * v]),
+                       "r"(packed[4 * v + 1]), "r"(packed[4 * v + 2]), "r"(packed[4 * v + 3])
+                       : "memory");
         }
       }
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        // this warp's 32 rows; rows past M and columns past Nc are not written
+#pragma unroll
+        for (int c = 0; c < BN / 64; ++c)
+          ptx::tma_store_3d(&tmC, base + c * (C::kBM * 128) + warp * 32 * 128, n0 + 64 * c, m0 + warp * 32, z);
+        ptx::bulk_commit_group();
+        ptx::bulk_wait_group_read0();
+      }
+      __syncwarp();
     }
   }
 
@@ -223,24 +234,42 @@ __global__ void __launch_bounds__(GemmCfg<BN, B_KMAJOR>::kThreads, 1)
 }
 
 // Row softmax in place: P[r] = bf16(e^{S[r] - m} / l) computed in fp32 from
-// the bf16 scores, LSE[r] = m + ln l. One CTA of 256 threads per row; rows
-// have n valid columns and a stride of ld elements.
-__global__ void __launch_bounds__(256) softmax_rows_kernel(__nv_bfloat16* S, float* LSE, int n, int ld) {
-  const size_t r = blockIdx.x;
-  __nv_bfloat16* row = S + r * static_cast<size_t>(ld);
-  __shared__ float red_m[8], red_l[8];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // pass 1: online max and sum of exponentials
-  float m = -INFINITY, l = 0.f;
-  for (int i = tid; i < n; i += 256) {
-    const float x = __bfloat162float(row[i]);
-    if (x > m) {
-      l = l * expf(m - x) + 1.f;
-      m = x;
-    } else {
-      l += expf(x - m);
-    }
+// the bf16 scores, LSE[r] = m + ln l. One warp per row (8 rows per 256-thread
+// block), 16-byte loads and stores; rows have n valid columns and a stride of
+// ld elements (a multiple of 64). Pass 1 keeps an online max and sum per lane
+// and merges them across the warp; pass 2 reads the row again and writes P
+// over it. (Keeping the row in shared memory or registers to save the second
+// read measured slower on GB300: fewer resident warps, less in flight.)
+__device__ __forceinline__ void softmax_absorb8(const uint4& u, float& m, float& l) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+  float x[8];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = __bfloat1622float2(h[e]);
+    x[2 * e] = f.x;
+    x[2 * e + 1] = f.y;
   }
+  float mx = x[0];
+#pragma unroll
+  for (int e = 1; e < 8; ++e) mx = fmaxf(mx, x[e]);
+  if (mx > m) {
+    l = (m == -INFINITY) ? 0.f : l * expf(m - mx);
+    m = mx;
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) l += expf(x[e] - m);
+}
+
+__device__ __forceinline__ void softmax_absorb1(float x, float& m, float& l) {
+  if (x > m) {
+    l = (m == -INFINITY) ? 1.f : l * expf(m - x) + 1.f;
+    m = x;
+  } else {
+    l += expf(x - m);
+  }
+}
+
+__device__ __forceinline__ void softmax_warp_merge(float& m, float& l) {
   for (int off = 16; off > 0; off >>= 1) {
     const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
     const float l2 = __shfl_xor_sync(0xffffffffu, l, off);
@@ -248,19 +277,34 @@ __global__ void __launch_bounds__(256) softmax_rows_kernel(__nv_bfloat16* S, flo
     l = (m == -INFINITY ? 0.f : l * expf(m - mn)) + (m2 == -INFINITY ? 0.f : l2 * expf(m2 - mn));
     m = mn;
   }
-  if (lane == 0) {
-    red_m[warp] = m;
-    red_l[warp] = l;
+}
+
+__device__ __forceinline__ uint4 softmax_emit8(uint4 u, float m, float inv) {
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = __bfloat1622float2(h[e]);
+    h[e] = __floats2bfloat162_rn(expf(f.x - m) * inv, expf(f.y - m) * inv);
   }
-  __syncthreads();
-  float mt = red_m[0];
-  for (int w = 1; w < 8; ++w) mt = fmaxf(mt, red_m[w]);
-  float lt = 0.f;
-  for (int w = 0; w < 8; ++w) lt += red_m[w] == -INFINITY ? 0.f : red_l[w] * expf(red_m[w] - mt);
-  // pass 2: write P over S
-  const float inv = 1.f / lt;
-  for (int i = tid; i < n; i += 256) row[i] = __float2bfloat16_rn(expf(__bfloat162float(row[i]) - mt) * inv);
-  if (tid == 0) LSE[r] = mt + logf(lt);
+  return u;
+}
+
+__global__ void __launch_bounds__(256) softmax_rows_kernel(__nv_bfloat16* S, float* LSE, long long rows, int n,
+                                                           int ld) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long r = static_cast<long long>(blockIdx.x) * 8 + warp;
+  if (r >= rows) return;
+  __nv_bfloat16* row = S + r * static_cast<size_t>(ld);
+  float m = -INFINITY, l = 0.f;
+  const int n8 = n & ~7;
+  for (int i = lane * 8; i < n8; i += 256) softmax_absorb8(*reinterpret_cast<const uint4*>(row + i), m, l);
+  for (int i = n8 + lane; i < n; i += 32) softmax_absorb1(__bfloat162float(row[i]), m, l);
+  softmax_warp_merge(m, l);
+  const float inv = 1.f / l;
+  for (int i = lane * 8; i < n8; i += 256)
+    *reinterpret_cast<uint4*>(row + i) = softmax_emit8(*reinterpret_cast<const uint4*>(row + i), m, inv);
+  for (int i = n8 + lane; i < n; i += 32) row[i] = __float2bfloat16_rn(expf(__bfloat162float(row[i]) - m) * inv);
+  if (lane == 0) LSE[r] = m + logf(l);
 }
 
 }  // namespace naive
