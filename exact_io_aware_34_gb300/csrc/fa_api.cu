@@ -433,7 +433,7 @@ fa_status_t bwd_impl(const void* Q, const void* K, const void* V, const void* O,
 
 // ---------------------------------------------------------------- shared K/V heads, short queries
 struct KvPlan {
-  int G, hp, tiles_per_group, n_kv_blocks, blocks_per_split, num_splits;
+  int G, hp, box_q, q_blocks, tiles_per_group, n_kv_blocks, blocks_per_split, num_splits;
 };
 
 int device_sm_count() {
@@ -443,15 +443,24 @@ int device_sm_count() {
   return sms;
 }
 
-// Packing and key split of the short-query path (N_q <= 128). With
-// num_splits <= 0 the split count fills one wave of CTAs (two per SM); it
-// is capped by the number of key blocks, and ranges are whole blocks with
-// no empty range.
+// Packing and key split of the short-query kernel. A tile is 128 query rows:
+// for N_q <= 128 the rows of min(G, 128 / N_q) heads of a group, for
+// N_q > 128 one 128-row block of one head. With num_splits <= 0 the split
+// count fills one wave of CTAs (two per SM); it is capped by the number of
+// key blocks, and ranges are whole blocks with no empty range.
 KvPlan kv_plan(int B, int H, int H_kv, int N_q, int N_kv, int num_splits) {
   KvPlan k;
   k.G = H / H_kv;
-  k.hp = std::min(k.G, 128 / N_q);
-  k.tiles_per_group = (k.G + k.hp - 1) / k.hp;
+  if (N_q <= 128) {
+    k.hp = std::min(k.G, 128 / N_q);
+    k.box_q = N_q;
+    k.q_blocks = 1;
+  } else {
+    k.hp = 1;
+    k.box_q = 128;
+    k.q_blocks = (N_q + 127) / 128;
+  }
+  k.tiles_per_group = (k.G + k.hp - 1) / k.hp * k.q_blocks;
   k.n_kv_blocks = (N_kv + 127) / 128;
   int s = num_splits;
   if (s <= 0) {
@@ -464,6 +473,30 @@ KvPlan kv_plan(int B, int H, int H_kv, int N_q, int N_kv, int num_splits) {
   k.blocks_per_split = (k.n_kv_blocks + s - 1) / s;
   k.num_splits = (k.n_kv_blocks + k.blocks_per_split - 1) / k.blocks_per_split;
   return k;
+}
+
+// Which kernel runs fa_fwd_kv. Short query blocks (N_q <= 128) take the
+// short-query kernel. Long ones take the fused forward kernel (two query
+// tiles per CTA, one CTA per SM, no split) when num_splits is 1, and with
+// num_splits = 0 whenever its CTAs fill more than three quarters of the SMs;
+// otherwise the short-query kernel with one 128-row query tile per CTA and a
+// key split fills the device. Both full, the short-query kernel runs long
+// query blocks at about 0.8 of the fused kernel's rate.
+struct KvRoute {
+  bool fused;
+  KvPlan plan;
+};
+
+KvRoute kv_route(int B, int H, int H_kv, int N_q, int N_kv, int num_splits) {
+  KvRoute r{false, kv_plan(B, H, H_kv, N_q, N_kv, num_splits)};
+  if (N_q <= 128) return r;
+  if (num_splits == 1) {
+    r.fused = true;
+  } else if (num_splits <= 0) {
+    const long long fused_ctas = static_cast<long long>(B) * H * ((N_q + 255) / 256);
+    r.fused = 4 * fused_ctas > 3LL * device_sm_count() || r.plan.num_splits <= 1;
+  }
+  return r;
 }
 
 size_t kv_workspace_bytes(int B, int H, int N_q, int d, const KvPlan& k) {
@@ -521,7 +554,7 @@ fa_status_t decode_launch(const void* Q, const void* K, const void* V, void* O, 
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(N_q),
                           static_cast<cuuint64_t>(B) * H};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(HD) * 2, static_cast<cuuint64_t>(N_q) * HD * 2};
-    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(N_q), static_cast<cuuint32_t>(k.hp)};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(k.box_q), static_cast<cuuint32_t>(k.hp)};
     cuuint32_t estr[3] = {1, 1, 1};
     if (fn(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(Q), dims, strides, box, estr,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -543,6 +576,8 @@ fa_status_t decode_launch(const void* Q, const void* K, const void* V, void* O, 
   p.H_kv = H_kv;
   p.G = k.G;
   p.hp = k.hp;
+  p.box_q = k.box_q;
+  p.q_blocks = k.q_blocks;
   p.tiles_per_group = k.tiles_per_group;
   p.n_kv_blocks = k.n_kv_blocks;
   p.blocks_per_split = k.blocks_per_split;
@@ -568,13 +603,14 @@ fa_status_t kv_impl(const void* Q, const void* K, const void* V, void* O, float*
                     int drop_load, unsigned long long timeout_ns, cudaStream_t stream) {
   fa_status_t st = kv_check(Q, K, V, O, LSE, B, H, H_kv, N_q, N_kv, d, scale);
   if (st != FA_OK) return st;
-  if (N_q > 128) {
+  const KvRoute route = kv_route(B, H, H_kv, N_q, N_kv, num_splits);
+  if (route.fused) {
     // Long query blocks: the fused forward kernel with the K/V head mapping.
-    if (num_splits > 1) return FA_ERR_UNSUPPORTED;
     if (d == 64) return launch<64>(Q, K, V, O, LSE, B, H, H_kv, N_q, N_kv, scale, drop_load, timeout_ns, stream);
     return launch<128>(Q, K, V, O, LSE, B, H, H_kv, N_q, N_kv, scale, drop_load, timeout_ns, stream);
   }
-  const KvPlan k = kv_plan(B, H, H_kv, N_q, N_kv, num_splits);
+  const KvPlan& k = route.plan;
+  if (static_cast<long long>(k.tiles_per_group) * k.num_splits > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;  // grid.x
   const size_t need = kv_workspace_bytes(B, H, N_q, d, k);
   if (need > 0) {
     if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 128 != 0 || workspace_bytes < need)
@@ -599,14 +635,14 @@ extern "C" {
 
 int fa_fwd_kv_num_splits(int B, int H, int H_kv, int N_q, int N_kv, int d) {
   if (B < 1 || H < 1 || H_kv < 1 || H % H_kv != 0 || N_q < 1 || N_kv < 1 || (d != 64 && d != 128)) return 0;
-  if (N_q > 128) return 1;
-  return kv_plan(B, H, H_kv, N_q, N_kv, 0).num_splits;
+  const KvRoute r = kv_route(B, H, H_kv, N_q, N_kv, 0);
+  return r.fused ? 1 : r.plan.num_splits;
 }
 
 size_t fa_fwd_kv_workspace_bytes(int B, int H, int H_kv, int N_q, int N_kv, int d, int num_splits) {
   if (B < 1 || H < 1 || H_kv < 1 || H % H_kv != 0 || N_q < 1 || N_kv < 1 || (d != 64 && d != 128)) return 0;
-  if (N_q > 128) return 0;
-  return kv_workspace_bytes(B, H, N_q, d, kv_plan(B, H, H_kv, N_q, N_kv, num_splits));
+  const KvRoute r = kv_route(B, H, H_kv, N_q, N_kv, num_splits);
+  return r.fused ? 0 : kv_workspace_bytes(B, H, N_q, d, r.plan);
 }
 
 fa_status_t fa_fwd_kv(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int H_kv,

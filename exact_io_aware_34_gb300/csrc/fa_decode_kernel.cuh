@@ -66,8 +66,10 @@ struct DecParams {
   int H;
   int H_kv;
   int G;                  // H / H_kv
-  int hp;                 // query heads packed per tile
-  int tiles_per_group;    // ceil(G / hp)
+  int hp;                 // query heads packed per tile (1 when N_q > 128)
+  int box_q;              // query rows per head in a tile: N_q, or 128 when N_q > 128
+  int q_blocks;           // 128-row query blocks per head: 1, or ceil(N_q / 128) when N_q > 128
+  int tiles_per_group;    // ceil(G / hp) * q_blocks
   int n_kv_blocks;
   int blocks_per_split;
   int num_splits;
@@ -98,9 +100,11 @@ __global__ void __launch_bounds__(DecCfg<HD>::kThreads, DecCfg<HD>::kCtasPerSm)
   const int split = blockIdx.x - tile * p.num_splits;
   const int kvh = blockIdx.y;
   const int b = blockIdx.z;
-  const int g0 = tile * p.hp;                                   // first query head of the group in this tile
+  const int head_tile = tile / p.q_blocks;
+  const int q0 = (tile - head_tile * p.q_blocks) * C::kBM;      // first query row of the tile
+  const int g0 = head_tile * p.hp;                              // first query head of the group in this tile
   const int nh = min(p.hp, p.G - g0);                           // query heads in this tile
-  const int rows = nh * p.N_q;                                  // tile rows that are real
+  const int rows = p.q_blocks == 1 ? nh * p.N_q : min(C::kBM, p.N_q - q0);   // tile rows that are real
   const int j0 = split * p.blocks_per_split;
   const int j1 = min(p.n_kv_blocks, j0 + p.blocks_per_split);
   const int n = j1 - j0;                                        // key blocks of this CTA (>= 1)
@@ -114,7 +118,7 @@ __global__ void __launch_bounds__(DecCfg<HD>::kThreads, DecCfg<HD>::kCtasPerSm)
 
   // Rows of the Q tile that no query fills are zero, so that their scores are
   // finite; they are never stored.
-  const int box_rows = p.hp * p.N_q;
+  const int box_rows = p.hp * p.box_q;
   for (int c = 0; c < C::kChunks; ++c)
     for (int i = threadIdx.x; i < (C::kBM - box_rows) * 8; i += C::kThreads)
       reinterpret_cast<uint4*>(q_generic + c * C::kChunkBytes + box_rows * 128)[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -156,7 +160,7 @@ __global__ void __launch_bounds__(DecCfg<HD>::kThreads, DecCfg<HD>::kCtasPerSm)
       const uint32_t q_full = ptx::smem_u32(&bar_q_full);
       ptx::mbar_arrive_expect_tx(q_full, C::kChunks * 128 * box_rows);
       for (int c = 0; c < C::kChunks; ++c)
-        ptx::tma_load_3d(sQ + c * C::kChunkBytes, &tmQ, q_full, c * 64, 0, bh_q0, pol_q);
+        ptx::tma_load_3d(sQ + c * C::kChunkBytes, &tmQ, q_full, c * 64, q0, bh_q0, pol_q);
       int issued = 0;
       bool ok = true;
       for (int jj = 0; jj < n && ok; ++jj) {
@@ -350,10 +354,10 @@ __global__ void __launch_bounds__(DecCfg<HD>::kThreads, DecCfg<HD>::kCtasPerSm)
     if (ok) ok = wait_warp_or_abort(ptx::smem_u32(&bar_o_full), 0, abort_ptr, p.timeout_ns, kRoleDecSoftmax);
     if (ok) {
       ptx::tc_fence_after();
-      // Row r of the tile is query row r % N_q of query head g0 + r / N_q.
+      // Row r of the tile is query row q0 + r % box_q of query head g0 + r / box_q.
       const bool in_range = row < rows;
-      const int hq = row / p.N_q;
-      const size_t grow = (static_cast<size_t>(bh_q0) + hq) * p.N_q + (row - hq * p.N_q);
+      const int hq = row / p.box_q;
+      const size_t grow = (static_cast<size_t>(bh_q0) + hq) * p.N_q + q0 + (row - hq * p.box_q);
       const float inv_l = 1.f / l;
       const float lse = (m_use * sl2 + __log2f(l)) * 0.69314718055994530942f;
       const size_t n_rows = static_cast<size_t>(gridDim.z) * p.H * p.N_q;

@@ -206,8 +206,10 @@ def fa_fwd_kv(q, k, v, o=None, lse=None, scale: float | None = None, num_splits:
 
     q: bf16 [B, H, N_q, d]; k, v: bf16 [B, H_kv, N_kv, d] with H a multiple of
     H_kv (query head h uses K/V head h // (H // H_kv)). Returns (o, lse).
-    ``num_splits`` = 0 lets the library choose the key split for N_q <= 128;
-    the workspace is allocated with torch when needed and not given.
+    ``num_splits`` = 0 lets the library choose the key split (none when the
+    fused forward kernel fills the device; see :func:`fa_fwd_kv_num_splits`),
+    1 forbids one; the workspace is allocated with torch when needed and not
+    given.
     """
     _check_kv(q, k, v)
     B, H, N_q, d = q.shape

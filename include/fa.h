@@ -153,30 +153,34 @@ fa_status_t fa_naive_fwd_noalloc(const void* Q, const void* K, const void* V, vo
  *   O      : device, bf16 [B, H, N_q, d], written.
  *   LSE    : device, float32 [B, H, N_q], written (natural log).
  *   Every query row attends to all N_kv keys (no mask).
- *   num_splits : N_q <= 128 only: the number of contiguous key ranges
- *            computed by separate CTAs and merged with the online-softmax rule
- *            ("Flash Attention (FA1)", derivation steps 4-5). 0 chooses one
- *            wave of CTAs (fa_fwd_kv_num_splits); values above the number of
- *            128-key blocks are capped. N_q > 128 takes the fused forward
- *            kernel and needs num_splits <= 1.
+ *   num_splits : the number of contiguous key ranges computed by separate
+ *            CTAs and merged with the online-softmax rule ("Flash Attention
+ *            (FA1)", derivation steps 4-5). 0 chooses (fa_fwd_kv_num_splits):
+ *            for N_q <= 128 one wave of CTAs; for N_q > 128 no split (the
+ *            fused forward kernel) unless that kernel would fill at most
+ *            three quarters of the SMs, else one wave. Values above the
+ *            number of 128-key blocks are capped. For N_q > 128, 1 always
+ *            takes the fused forward kernel (the same result as fa_fwd when
+ *            H_kv = H and N_q = N_kv).
  *   workspace, workspace_bytes : device memory of at least
  *            fa_fwd_kv_workspace_bytes(...) bytes, 128-byte aligned, not
  *            overlapping any other buffer; may be NULL when that is 0 (one
- *            split or N_q > 128).
- * For N_q <= 128 the query rows of the heads sharing a K/V head are packed
- * into one 128-row tile (min(H/H_kv, 128/N_q) heads per tile), so each K/V
- * tile is read once per group. Launches: one kernel, plus one merge kernel
- * when there is more than one split. Limits as for fa_fwd; FA_ERR_INVALID_ARG
- * also when H is not a multiple of H_kv or for a missing, misaligned, small or
- * overlapping workspace.
+ *            split or the fused forward kernel).
+ * The short-query kernel tiles 128 query rows: for N_q <= 128 the rows of
+ * the heads sharing a K/V head are packed into one tile (min(H/H_kv, 128/N_q)
+ * heads per tile), so each K/V tile is read once per group; for N_q > 128 a
+ * tile is one 128-row block of one head. Launches: one kernel, plus one merge
+ * kernel when there is more than one split. Limits as for fa_fwd;
+ * FA_ERR_INVALID_ARG also when H is not a multiple of H_kv or for a missing,
+ * misaligned, small or overlapping workspace.
  */
 fa_status_t fa_fwd_kv(const void* Q, const void* K, const void* V, void* O, float* LSE,
                       int B, int H, int H_kv, int N_q, int N_kv, int d, float scale,
                       int num_splits, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* fa_fwd_kv_num_splits -- the split count fa_fwd_kv uses when num_splits is 0
- * (1 when N_q > 128); 0 for invalid sizes. Depends on the current device's SM
- * count. */
+ * (1 when it takes the fused forward kernel); 0 for invalid sizes. Depends on
+ * the current device's SM count (148 when there is no device). */
 int fa_fwd_kv_num_splits(int B, int H, int H_kv, int N_q, int N_kv, int d);
 
 /* fa_fwd_kv_workspace_bytes -- workspace bytes fa_fwd_kv needs for these sizes
@@ -186,9 +190,10 @@ size_t fa_fwd_kv_workspace_bytes(int B, int H, int H_kv, int N_q, int N_kv, int 
 
 /*
  * fa_fwd_kv_fault_test -- TEST HOOK, not for production use. fa_fwd_kv with
- * every device-side wait limited to `timeout_ns`, and, when drop_load >= 0 and
- * N_q <= 128, the drop_load-th K/V tile load (K, V of a CTA's first block,
- * then of its second, ...) skipped in every CTA; as for fa_fwd_fault_test.
+ * every device-side wait limited to `timeout_ns`, and, when drop_load >= 0,
+ * the drop_load-th K/V tile load skipped in every CTA (in the short-query
+ * kernel: K, V of a CTA's first block, then of its second, ...; in the fused
+ * forward kernel as for fa_fwd_fault_test).
  */
 fa_status_t fa_fwd_kv_fault_test(const void* Q, const void* K, const void* V, void* O, float* LSE,
                                  int B, int H, int H_kv, int N_q, int N_kv, int d, float scale,

@@ -184,11 +184,26 @@ def test_kv_workspace_and_splits(lib):
     assert fa.fa_fwd_kv_workspace_bytes(1, 8, 2, 1, 4096, 128, 4) == 4 * 8 * 129 * 4
     assert fa.fa_fwd_kv_workspace_bytes(1, 8, 2, 1, 4096, 128, 1) == 0
     assert fa.fa_fwd_kv_workspace_bytes(1, 8, 2, 1, 200, 128, 9) == 2 * 8 * 129 * 4   # capped at 2 key blocks
-    assert fa.fa_fwd_kv_workspace_bytes(1, 8, 2, 300, 300, 128, 0) == 0                # long queries: no split
+    assert fa.fa_fwd_kv_workspace_bytes(1, 8, 2, 300, 300, 128, 1) == 0                # the fused kernel: no split
     assert fa.fa_fwd_kv_workspace_bytes(1, 8, 3, 1, 64, 128, 0) == 0                   # 8 % 3 != 0
     assert fa.fa_fwd_kv_num_splits(1, 8, 2, 1, 200, 128) in (1, 2)
     assert fa.fa_fwd_kv_num_splits(1, 8, 3, 1, 64, 128) == 0
-    assert fa.fa_fwd_kv_num_splits(1, 8, 2, 300, 300, 128) == 1
+    # long query blocks: 3 key ranges of 300 query rows of 8 heads
+    assert fa.fa_fwd_kv_workspace_bytes(1, 8, 2, 300, 300, 128, 3) == 3 * 8 * 300 * 129 * 4
+
+
+def test_kv_long_query_routing(lib):
+    """N_q > 128: the fused forward kernel (1 split, no workspace) when its
+    CTAs fill the device, else a key split over one wave of short-query CTAs."""
+    # 4 * 32 heads * 16 CTAs of 256 query rows = 2048 CTAs: fused
+    assert fa.fa_fwd_kv_num_splits(4, 32, 8, 4096, 4096, 128) == 1
+    assert fa.fa_fwd_kv_workspace_bytes(4, 32, 8, 4096, 4096, 128, 0) == 0
+    # 8 heads * 2 CTAs: 16 fused CTAs; 2 K/V heads * 4 heads * 4 query blocks = 32 short-query tiles
+    s = fa.fa_fwd_kv_num_splits(1, 8, 2, 512, 32768, 128)
+    assert 2 <= s <= 256
+    assert fa.fa_fwd_kv_workspace_bytes(1, 8, 2, 512, 32768, 128, 0) == s * 8 * 512 * 129 * 4
+    # one key block: nothing to split, the fused kernel
+    assert fa.fa_fwd_kv_num_splits(1, 8, 2, 512, 100, 64) == 1
 
 
 @pytest.mark.parametrize("kwargs,expect", [
@@ -205,7 +220,7 @@ def test_kv_workspace_and_splits(lib):
     (dict(O=A + GAP + 64), fa.FA_ERR_INVALID_ARG),               # O overlaps K
     (dict(L=A + 3 * GAP + 4), fa.FA_ERR_INVALID_ARG),            # LSE overlaps O
     (dict(Q=A + 8), fa.FA_ERR_INVALID_ARG),
-    (dict(Nq=300, Nkv=300, splits=2), fa.FA_ERR_UNSUPPORTED),    # no split for long query blocks
+    (dict(Nq=300, Nkv=300, splits=2, ws_bytes=2 * 8 * 300 * 129 * 4 - 1), fa.FA_ERR_INVALID_ARG),  # long queries, small
 ])
 def test_kv_host_side_rejections(lib, kwargs, expect):
     assert kv_call(lib, **kwargs) == expect

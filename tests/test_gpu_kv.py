@@ -88,18 +88,35 @@ def test_spiky_keys_with_splits():
     check_kv(q, k, v, 1 / math.sqrt(128), num_splits=6)
 
 
-# --- long query blocks with shared K/V heads (the fused forward kernel) -------------
+# --- long query blocks with shared K/V heads ----------------------------------------
+# num_splits = 1 takes the fused forward kernel; 0 (at these few heads) and
+# explicit counts take the short-query kernel with 128-row query tiles and a
+# key split.
+@pytest.mark.parametrize("num_splits", [1, 0, 5])
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("N_q,N_kv,G", [(300, 300, 4), (1000, 700, 2), (129, 2000, 8)])
-def test_long_queries(d, N_q, N_kv, G):
+@pytest.mark.parametrize("N_q,N_kv,G", [(300, 300, 4), (1000, 700, 2), (129, 2000, 8), (257, 129, 1)])
+def test_long_queries(d, N_q, N_kv, G, num_splits):
     q, k, v = inputs.make_kv(1, 2 * G, 2, N_q, N_kv, d, seed=N_q + N_kv + G + d)
-    check_kv(q, k, v, 1 / math.sqrt(d))
+    check_kv(q, k, v, 1 / math.sqrt(d), num_splits=num_splits)
+
+
+def test_long_query_split_is_chosen_for_few_heads():
+    """A chunk of 512 queries of 8 heads against 32k keys: the automatic
+    choice is a key split (the fused kernel would fill 16 SMs)."""
+    q, k, v = inputs.make_kv(1, 8, 2, 512, 32768, 128, seed=335)
+    splits = fa.fa_fwd_kv_num_splits(1, 8, 2, 512, 32768, 128)
+    assert splits > 1
+    err, o, lse = check_kv(q, k, v, 1 / math.sqrt(128))
+    o1, l1 = run_kv(q, k, v, 1 / math.sqrt(128), num_splits=1)
+    assert float((o.float() - o1.float()).abs().max()) <= 1e-2
+    assert float((lse - l1).abs().max()) <= 1e-4
+    print(splits, err)
 
 
 def test_kv_heads_equal_reduces_to_fa_fwd():
-    """H_kv = H and N_q = N_kv: the same result as fa_fwd, bit for bit."""
+    """H_kv = H and N_q = N_kv with one split: the same result as fa_fwd, bit for bit."""
     q, k, v = inputs.make_random(1, 4, 700, 128, seed=330)
-    o1, l1 = run_kv(q, k, v, 0.09)
+    o1, l1 = run_kv(q, k, v, 0.09, num_splits=1)
     o2, l2 = parity.run_gpu(q, k, v, 0.09)
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
     assert torch.equal(l1, l2)
@@ -114,12 +131,13 @@ def test_decode_workload_full():
 
 
 # --- failure path and rejections ---------------------------------------------------
+@pytest.mark.parametrize("N_q", [2, 300])
 @pytest.mark.parametrize("drop", [0, 1, 4])
-def test_kv_dropped_load_times_out_cleanly(drop):
-    q, k, v = (x.cuda() for x in inputs.make_kv(1, 8, 2, 2, 2000, 128, seed=340 + drop))
+def test_kv_dropped_load_times_out_cleanly(drop, N_q):
+    q, k, v = (x.cuda() for x in inputs.make_kv(1, 8, 2, N_q, 2000, 128, seed=340 + drop))
     o = torch.zeros_like(q)
-    lse = torch.zeros(1, 8, 2, device="cuda")
-    ws = torch.empty(fa.fa_fwd_kv_workspace_bytes(1, 8, 2, 2, 2000, 128, 3), dtype=torch.uint8, device="cuda")
+    lse = torch.zeros(1, 8, N_q, device="cuda")
+    ws = torch.empty(fa.fa_fwd_kv_workspace_bytes(1, 8, 2, N_q, 2000, 128, 3), dtype=torch.uint8, device="cuda")
     st = fa.fa_fwd_kv_fault_test(q, k, v, o, lse, 0.1, 3, ws, drop, 20_000_000)
     assert st == fa.FA_OK
     st, info = fa.fa_get_device_status()
