@@ -134,30 +134,31 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
 }
 
 // S-shaped product over the model dimension: D[128 x 128] = A B^T with A and
-// B two 128-row tiles in the K-major swizzled layout (k = 0 .. HD).
+// B two 128-row tiles in the K-major swizzled layout (k = 0 .. HD). Called by
+// the whole converged issuer warp (one elected lane issues).
 template <int HD>
 __device__ __forceinline__ void issue_tile_qk(uint32_t d_tmem, uint32_t a_tile, uint32_t b_tile) {
   using C = BwdCfg<HD>;
 #pragma unroll
   for (int kk = 0; kk < HD / 16; ++kk) {
     const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-    ptx::mma_ss(d_tmem, ptx::desc_kmajor_sw128(a_tile + off), ptx::desc_kmajor_sw128(b_tile + off), C::kIdescS,
-                kk > 0 ? 1u : 0u);
+    ptx::mma_ss_warp(d_tmem, ptx::desc_kmajor_sw128(a_tile + off), ptx::desc_kmajor_sw128(b_tile + off),
+                     C::kIdescS, kk > 0 ? 1u : 0u);
   }
 }
 
 // Accumulating product over the 128 streamed rows: D[128 x HD] += A B with A
 // packed bf16 in TMEM (rows 64h .. 64h+63 of the streamed block at column
 // a_col + kHalf * h, 16 rows per 8 columns) and B a 128 x HD tile read
-// MN-major from shared memory.
+// MN-major from shared memory. Called by the whole converged issuer warp.
 template <int HD, int kHalf>
 __device__ __forceinline__ void issue_tile_acc(uint32_t d_tmem, uint32_t a_col, uint32_t b_tile, bool accumulate) {
   using C = BwdCfg<HD>;
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
     const uint64_t b_desc = ptx::desc_mnmajor_sw128(b_tile + kk * 16 * 128, C::kChunkBytes);
-    ptx::mma_ts(d_tmem, a_col + kHalf * (kk >> 2) + 8 * (kk & 3), b_desc, C::kIdescAcc,
-                (accumulate || kk > 0) ? 1u : 0u);
+    ptx::mma_ts_warp(d_tmem, a_col + kHalf * (kk >> 2) + 8 * (kk & 3), b_desc, C::kIdescAcc,
+                     (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -318,43 +319,45 @@ __global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
     __syncwarp();
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this converged (warp-uniform waits, one elected
+    // lane issues each tcgen05 instruction).
+    {
       auto k_tile = [&](int j) { return sK + (j % D::kKSlots) * C::kTileBytes; };
       auto v_tile = [&](int j) { return sV + (j % D::kVSlots) * C::kTileBytes; };
       // S_j = Q K_j^T and dP_j = dO V_j^T, after K_j and V_j have landed.
       auto issue_sdp = [&](int j) -> bool {
-        if (!wait_or_abort(ptx::smem_u32(&bar_k_full[j % D::kKSlots]), (j / D::kKSlots) & 1, abort_ptr,
+        if (!wait_warp_or_abort(ptx::smem_u32(&bar_k_full[j % D::kKSlots]), (j / D::kKSlots) & 1, abort_ptr,
                            p.timeout_ns, kRoleDqMma))
           return false;
-        if (!wait_or_abort(ptx::smem_u32(&bar_v_full[j % D::kVSlots]), (j / D::kVSlots) & 1, abort_ptr,
+        if (!wait_warp_or_abort(ptx::smem_u32(&bar_v_full[j % D::kVSlots]), (j / D::kVSlots) & 1, abort_ptr,
                            p.timeout_ns, kRoleDqMma))
           return false;
         ptx::tc_fence_after();
         issue_tile_qk<HD>(tmem_base + D::kColS, sQ, k_tile(j));
         issue_tile_qk<HD>(tmem_base + D::kColP, sdO, v_tile(j));
-        ptx::mma_commit(ptx::smem_u32(&bar_v_empty[j % D::kVSlots]));
-        ptx::mma_commit(ptx::smem_u32(&bar_s_full));
+        ptx::mma_commit_warp(ptx::smem_u32(&bar_v_empty[j % D::kVSlots]));
+        ptx::mma_commit_warp(ptx::smem_u32(&bar_s_full));
         return true;
       };
-      bool ok = wait_or_abort(ptx::smem_u32(&bar_in_full), 0, abort_ptr, p.timeout_ns, kRoleDqMma);
+      bool ok = wait_warp_or_abort(ptx::smem_u32(&bar_in_full), 0, abort_ptr, p.timeout_ns, kRoleDqMma);
       if (ok) ok = issue_sdp(0);
       for (int j = 0; j < n && ok; ++j) {
         if (j + 1 < n) {
-          ok = wait_or_abort(ptx::smem_u32(&bar_dp_free), j & 1, abort_ptr, p.timeout_ns, kRoleDqMma);
+          ok = wait_warp_or_abort(ptx::smem_u32(&bar_dp_free), j & 1, abort_ptr, p.timeout_ns, kRoleDqMma);
           if (!ok) break;
           ok = issue_sdp(j + 1);
           if (!ok) break;
         }
-        ok = wait_or_abort(ptx::smem_u32(&bar_p_full[j & 1]), (j >> 1) & 1, abort_ptr, p.timeout_ns, kRoleDqMma);
+        ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_full[j & 1]), (j >> 1) & 1, abort_ptr, p.timeout_ns, kRoleDqMma);
         if (!ok) break;
         ptx::tc_fence_after();
         issue_tile_acc<HD, 32>(tmem_base + D::kColDQ, tmem_base + D::kColDS + 64u * (j & 1), k_tile(j), j > 0);
-        ptx::mma_commit(ptx::smem_u32(&bar_k_empty[j % D::kKSlots]));
+        ptx::mma_commit_warp(ptx::smem_u32(&bar_k_empty[j % D::kKSlots]));
       }
       if (ok) {
-        ptx::mma_commit(ptx::smem_u32(&bar_acc_full));
+        ptx::mma_commit_warp(ptx::smem_u32(&bar_acc_full));
       } else {
-        ptx::mma_commit(ptx::smem_u32(&bar_drain));
+        ptx::mma_commit_warp(ptx::smem_u32(&bar_drain));
         drain_wait(ptx::smem_u32(&bar_drain), 0, p.timeout_ns);
       }
     }
@@ -550,43 +553,45 @@ __global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
     __syncwarp();
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this converged (warp-uniform waits, one elected
+    // lane issues each tcgen05 instruction).
+    {
       auto region = [&](int i) { return tmem_base + kColR + 128u * static_cast<uint32_t>(i & 1); };
       auto q_tile = [&](int i) { return sRing + (i % C::kStages) * C::kPairBytes; };
-      bool ok = wait_or_abort(ptx::smem_u32(&bar_kv_full), 0, abort_ptr, p.timeout_ns, kRoleDkvMma);
-      if (ok) ok = wait_or_abort(ptx::smem_u32(&bar_in_full[0]), 0, abort_ptr, p.timeout_ns, kRoleDkvMma);
+      bool ok = wait_warp_or_abort(ptx::smem_u32(&bar_kv_full), 0, abort_ptr, p.timeout_ns, kRoleDkvMma);
+      if (ok) ok = wait_warp_or_abort(ptx::smem_u32(&bar_in_full[0]), 0, abort_ptr, p.timeout_ns, kRoleDkvMma);
       if (ok) {
         ptx::tc_fence_after();
         issue_tile_qk<HD>(region(0), sK, q_tile(0));                   // S_0^T = K Q_0^T
         issue_tile_qk<HD>(region(1), sV, q_tile(0) + C::kTileBytes);   // dP_0^T = V dO_0^T
-        ptx::mma_commit(ptx::smem_u32(&bar_s_full));
+        ptx::mma_commit_warp(ptx::smem_u32(&bar_s_full));
       }
       for (int i = 0; i < n && ok; ++i) {
         if (i + 1 < n) {
           const int s1 = (i + 1) % C::kStages;
-          ok = wait_or_abort(ptx::smem_u32(&bar_in_full[s1]), ((i + 1) / C::kStages) & 1, abort_ptr, p.timeout_ns,
+          ok = wait_warp_or_abort(ptx::smem_u32(&bar_in_full[s1]), ((i + 1) / C::kStages) & 1, abort_ptr, p.timeout_ns,
                              kRoleDkvMma);
           if (!ok) break;
-          ok = wait_or_abort(ptx::smem_u32(&bar_dp_free), i & 1, abort_ptr, p.timeout_ns, kRoleDkvMma);
+          ok = wait_warp_or_abort(ptx::smem_u32(&bar_dp_free), i & 1, abort_ptr, p.timeout_ns, kRoleDkvMma);
           if (!ok) break;
           ptx::tc_fence_after();
           issue_tile_qk<HD>(region(i + 1), sK, q_tile(i + 1));          // S_{i+1}^T
         }
-        ok = wait_or_abort(ptx::smem_u32(&bar_p_full), i & 1, abort_ptr, p.timeout_ns, kRoleDkvMma);
+        ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_full), i & 1, abort_ptr, p.timeout_ns, kRoleDkvMma);
         if (!ok) break;
         ptx::tc_fence_after();
         issue_tile_acc<HD, 64>(tmem_base + kColDV, region(i), q_tile(i) + C::kTileBytes, i > 0);   // dV += P^T dO_i
         issue_tile_acc<HD, 64>(tmem_base + kColDK, region(i) + 32, q_tile(i), i > 0);             // dK += dS^T Q_i
-        ptx::mma_commit(ptx::smem_u32(&bar_in_empty[i % C::kStages]));
+        ptx::mma_commit_warp(ptx::smem_u32(&bar_in_empty[i % C::kStages]));
         if (i + 1 < n) {
           issue_tile_qk<HD>(region(i), sV, q_tile(i + 1) + C::kTileBytes);   // dP_{i+1}^T
-          ptx::mma_commit(ptx::smem_u32(&bar_s_full));
+          ptx::mma_commit_warp(ptx::smem_u32(&bar_s_full));
         }
       }
       if (ok) {
-        ptx::mma_commit(ptx::smem_u32(&bar_acc_full));
+        ptx::mma_commit_warp(ptx::smem_u32(&bar_acc_full));
       } else {
-        ptx::mma_commit(ptx::smem_u32(&bar_drain));
+        ptx::mma_commit_warp(ptx::smem_u32(&bar_drain));
         drain_wait(ptx::smem_u32(&bar_drain), 0, p.timeout_ns);
       }
     }

@@ -192,26 +192,28 @@ __global__ void __launch_bounds__(DecCfg<HD>::kThreads, DecCfg<HD>::kCtasPerSm)
     __syncwarp();
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this converged (warp-uniform waits, one elected
+    // lane issues each tcgen05 instruction).
+    {
       auto kv_wait = [&](int it) {
-        return wait_or_abort(ptx::smem_u32(&bar_kv_full[it % C::kStages]), (it / C::kStages) & 1, abort_ptr,
+        return wait_warp_or_abort(ptx::smem_u32(&bar_kv_full[it % C::kStages]), (it / C::kStages) & 1, abort_ptr,
                              p.timeout_ns, kRoleDecMma);
       };
-      bool ok = wait_or_abort(ptx::smem_u32(&bar_q_full), 0, abort_ptr, p.timeout_ns, kRoleDecMma);
+      bool ok = wait_warp_or_abort(ptx::smem_u32(&bar_q_full), 0, abort_ptr, p.timeout_ns, kRoleDecMma);
       for (int jj = 0; jj < n && ok; ++jj) {
         if (jj > 0) {
           // O += P V for the previous block (P sits in the S columns).
-          ok = wait_or_abort(ptx::smem_u32(&bar_p_full), (jj - 1) & 1, abort_ptr, p.timeout_ns, kRoleDecMma);
+          ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_full), (jj - 1) & 1, abort_ptr, p.timeout_ns, kRoleDecMma);
           if (ok) ok = kv_wait(2 * (jj - 1) + 1);
           if (!ok) break;
           ptx::tc_fence_after();
           const uint32_t v_tile = sKV + ((2 * (jj - 1) + 1) % C::kStages) * C::kTileBytes;
 #pragma unroll
           for (int kk = 0; kk < C::kBN / 16; ++kk)
-            ptx::mma_ts(tmem_base + C::kColO, tmem_base + C::kColS + kk * 8,
-                        ptx::desc_mnmajor_sw128(v_tile + kk * 16 * 128, C::kChunkBytes), C::kIdescPV,
-                        (jj > 1 || kk > 0) ? 1u : 0u);
-          ptx::mma_commit(ptx::smem_u32(&bar_kv_empty[(2 * (jj - 1) + 1) % C::kStages]));
+            ptx::mma_ts_warp(tmem_base + C::kColO, tmem_base + C::kColS + kk * 8,
+                             ptx::desc_mnmajor_sw128(v_tile + kk * 16 * 128, C::kChunkBytes), C::kIdescPV,
+                             (jj > 1 || kk > 0) ? 1u : 0u);
+          ptx::mma_commit_warp(ptx::smem_u32(&bar_kv_empty[(2 * (jj - 1) + 1) % C::kStages]));
         }
         ok = kv_wait(2 * jj);
         if (!ok) break;
@@ -220,30 +222,30 @@ __global__ void __launch_bounds__(DecCfg<HD>::kThreads, DecCfg<HD>::kCtasPerSm)
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-          ptx::mma_ss(tmem_base + C::kColS, ptx::desc_kmajor_sw128(sQ + off), ptx::desc_kmajor_sw128(k_tile + off),
-                      C::kIdescQK, kk > 0 ? 1u : 0u);
+          ptx::mma_ss_warp(tmem_base + C::kColS, ptx::desc_kmajor_sw128(sQ + off),
+                           ptx::desc_kmajor_sw128(k_tile + off), C::kIdescQK, kk > 0 ? 1u : 0u);
         }
-        ptx::mma_commit(ptx::smem_u32(&bar_s_full));
-        ptx::mma_commit(ptx::smem_u32(&bar_kv_empty[(2 * jj) % C::kStages]));
+        ptx::mma_commit_warp(ptx::smem_u32(&bar_s_full));
+        ptx::mma_commit_warp(ptx::smem_u32(&bar_kv_empty[(2 * jj) % C::kStages]));
       }
       if (ok) {
         // The last block's P V.
-        ok = wait_or_abort(ptx::smem_u32(&bar_p_full), (n - 1) & 1, abort_ptr, p.timeout_ns, kRoleDecMma);
+        ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_full), (n - 1) & 1, abort_ptr, p.timeout_ns, kRoleDecMma);
         if (ok) ok = kv_wait(2 * (n - 1) + 1);
         if (ok) {
           ptx::tc_fence_after();
           const uint32_t v_tile = sKV + ((2 * (n - 1) + 1) % C::kStages) * C::kTileBytes;
 #pragma unroll
           for (int kk = 0; kk < C::kBN / 16; ++kk)
-            ptx::mma_ts(tmem_base + C::kColO, tmem_base + C::kColS + kk * 8,
-                        ptx::desc_mnmajor_sw128(v_tile + kk * 16 * 128, C::kChunkBytes), C::kIdescPV,
-                        (n > 1 || kk > 0) ? 1u : 0u);
-          ptx::mma_commit(ptx::smem_u32(&bar_o_full));
-          ptx::mma_commit(ptx::smem_u32(&bar_kv_empty[(2 * (n - 1) + 1) % C::kStages]));
+            ptx::mma_ts_warp(tmem_base + C::kColO, tmem_base + C::kColS + kk * 8,
+                             ptx::desc_mnmajor_sw128(v_tile + kk * 16 * 128, C::kChunkBytes), C::kIdescPV,
+                             (n > 1 || kk > 0) ? 1u : 0u);
+          ptx::mma_commit_warp(ptx::smem_u32(&bar_o_full));
+          ptx::mma_commit_warp(ptx::smem_u32(&bar_kv_empty[(2 * (n - 1) + 1) % C::kStages]));
         }
       }
       if (!ok) {
-        ptx::mma_commit(ptx::smem_u32(&bar_drain));
+        ptx::mma_commit_warp(ptx::smem_u32(&bar_drain));
         drain_wait(ptx::smem_u32(&bar_drain), 0, p.timeout_ns);
       }
     }

@@ -256,70 +256,72 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
     __syncwarp();
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      bool ok = wait_or_abort(ptx::smem_u32(&bar_q_full), 0, abort_ptr, p.timeout_ns, kRoleMma);
+    // The whole warp runs this code converged: waits are warp-uniform and one
+    // elected lane issues every tcgen05 instruction. A lone diverged lane
+    // issues far more slowly while the softmax warps of its sub-partition
+    // compete for issue slots.
+    bool ok = wait_warp_or_abort(ptx::smem_u32(&bar_q_full), 0, abort_ptr, p.timeout_ns, kRoleMma);
+    ptx::tc_fence_after();
+    // P V for query tile t and key block jj (P_t sits in the S_t columns).
+    auto issue_pv = [&](int t, int jj) {
+      const int it = 2 * jj + 1;
+      const uint32_t v_tile = sKV + (it % C::kStages) * C::kTileBytes;
+      const uint32_t d_tmem = tmem_base + C::kColO + HD * t;
+      const uint32_t a_tmem = tmem_base + C::kColS + 128 * t;
+#pragma unroll
+      for (int kk = 0; kk < C::kBN / 16; ++kk) {
+        const uint64_t b_desc = ptx::desc_mnmajor_sw128(v_tile + kk * 16 * 128, C::kChunkBytes);
+        ptx::mma_ts_warp(d_tmem, a_tmem + kk * 8, b_desc, C::kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
+      }
+    };
+    // S_t = Q_t K_j^T.
+    auto issue_qk = [&](int t, int j) {
+      const int it = 2 * j;
+      const uint32_t k_tile = sKV + (it % C::kStages) * C::kTileBytes;
+      const uint32_t q_tile = sQ + t * C::kTileBytes;
+      const uint32_t d_tmem = tmem_base + C::kColS + 128 * t;
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+        ptx::mma_ss_warp(d_tmem, ptx::desc_kmajor_sw128(q_tile + off), ptx::desc_kmajor_sw128(k_tile + off),
+                         C::kIdescQK, kk > 0 ? 1u : 0u);
+      }
+    };
+    // K_0 is waited for here; every later K_{j+1} and V_j is waited for by
+    // the softmax warps before their hand-off for block j (p_full), so the
+    // p_full waits below imply those tiles have landed. An mbarrier wait in
+    // this warp stalls the queued tensor-core work, so it does as few as it
+    // can.
+    if (ok) ok = wait_warp_or_abort(ptx::smem_u32(&bar_kv_full[0]), 0, abort_ptr, p.timeout_ns, kRoleMma);
+    for (int j = 0; j < n_kv && ok; ++j) {
+      const int itK = 2 * j;
       ptx::tc_fence_after();
-      // P V for query tile t and key block jj (P_t sits in the S_t columns).
-      auto issue_pv = [&](int t, int jj) {
-        const int it = 2 * jj + 1;
-        const uint32_t v_tile = sKV + (it % C::kStages) * C::kTileBytes;
-        const uint32_t d_tmem = tmem_base + C::kColO + HD * t;
-        const uint32_t a_tmem = tmem_base + C::kColS + 128 * t;
-#pragma unroll
-        for (int kk = 0; kk < C::kBN / 16; ++kk) {
-          const uint64_t b_desc = ptx::desc_mnmajor_sw128(v_tile + kk * 16 * 128, C::kChunkBytes);
-          ptx::mma_ts(d_tmem, a_tmem + kk * 8, b_desc, C::kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
-        }
-      };
-      // S_t = Q_t K_j^T.
-      auto issue_qk = [&](int t, int j) {
-        const int it = 2 * j;
-        const uint32_t k_tile = sKV + (it % C::kStages) * C::kTileBytes;
-        const uint32_t q_tile = sQ + t * C::kTileBytes;
-        const uint32_t d_tmem = tmem_base + C::kColS + 128 * t;
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-          ptx::mma_ss(d_tmem, ptx::desc_kmajor_sw128(q_tile + off), ptx::desc_kmajor_sw128(k_tile + off),
-                      C::kIdescQK, kk > 0 ? 1u : 0u);
-        }
-      };
-      // K_0 is waited for here; every later K_{j+1} and V_j is waited for by
-      // the softmax warps before their hand-off for block j (p_full), so the
-      // p_full waits below imply those tiles have landed. An mbarrier wait in
-      // this thread stalls the queued tensor-core work, so it does as few as
-      // it can.
-      if (ok) ok = wait_or_abort(ptx::smem_u32(&bar_kv_full[0]), 0, abort_ptr, p.timeout_ns, kRoleMma);
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int itK = 2 * j;
-        ptx::tc_fence_after();
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (j > 0) {
-            ok = wait_or_abort(ptx::smem_u32(&bar_p_full[t]), (j - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
-            if (!ok) break;
-            ptx::tc_fence_after();
-            issue_pv(t, j - 1);
-            if (t == 1) ptx::mma_commit(ptx::smem_u32(&bar_kv_empty[(2 * (j - 1) + 1) % C::kStages]));
-          }
-          issue_qk(t, j);
-          ptx::mma_commit(ptx::smem_u32(&bar_s_full[t]));
-        }
-        if (ok) ptx::mma_commit(ptx::smem_u32(&bar_kv_empty[itK % C::kStages]));
-      }
-      // The last key block's P V.
       for (int t = 0; t < 2 && ok; ++t) {
-        ok = wait_or_abort(ptx::smem_u32(&bar_p_full[t]), (n_kv - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
-        if (!ok) break;
-        ptx::tc_fence_after();
-        issue_pv(t, n_kv - 1);
-        ptx::mma_commit(ptx::smem_u32(&bar_o_full[t]));
-        if (t == 1) ptx::mma_commit(ptx::smem_u32(&bar_kv_empty[(2 * (n_kv - 1) + 1) % C::kStages]));
+        if (j > 0) {
+          ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_full[t]), (j - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          issue_pv(t, j - 1);
+          if (t == 1) ptx::mma_commit_warp(ptx::smem_u32(&bar_kv_empty[(2 * (j - 1) + 1) % C::kStages]));
+        }
+        issue_qk(t, j);
+        ptx::mma_commit_warp(ptx::smem_u32(&bar_s_full[t]));
       }
-      if (!ok) {
-        // Wait for every MMA already issued before TMEM is freed.
-        ptx::mma_commit(ptx::smem_u32(&bar_drain));
-        drain_wait(ptx::smem_u32(&bar_drain), 0, p.timeout_ns);
-      }
+      if (ok) ptx::mma_commit_warp(ptx::smem_u32(&bar_kv_empty[itK % C::kStages]));
+    }
+    // The last key block's P V.
+    for (int t = 0; t < 2 && ok; ++t) {
+      ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_full[t]), (n_kv - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      issue_pv(t, n_kv - 1);
+      ptx::mma_commit_warp(ptx::smem_u32(&bar_o_full[t]));
+      if (t == 1) ptx::mma_commit_warp(ptx::smem_u32(&bar_kv_empty[(2 * (n_kv - 1) + 1) % C::kStages]));
+    }
+    if (!ok) {
+      // Wait for every MMA already issued before TMEM is freed.
+      ptx::mma_commit_warp(ptx::smem_u32(&bar_drain));
+      drain_wait(ptx::smem_u32(&bar_drain), 0, p.timeout_ns);
     }
     __syncwarp();
   } else {
