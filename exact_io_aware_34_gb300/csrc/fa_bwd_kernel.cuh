@@ -139,12 +139,12 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
 template <int HD>
 __device__ __forceinline__ void issue_tile_qk(uint32_t d_tmem, uint32_t a_tile, uint32_t b_tile) {
   using C = BwdCfg<HD>;
-#pragma unroll
-  for (int kk = 0; kk < HD / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-    ptx::mma_ss_warp(d_tmem, ptx::desc_kmajor_sw128(a_tile + off), ptx::desc_kmajor_sw128(b_tile + off),
-                     C::kIdescS, kk > 0 ? 1u : 0u);
-  }
+  static_assert(C::kChunkBytes == 16384, "128-row tiles of 128-byte rows per chunk");
+  const uint64_t a_desc = ptx::desc_kmajor_sw128(a_tile), b_desc = ptx::desc_kmajor_sw128(b_tile);
+  if constexpr (HD == 128)
+    ptx::mma_ss_k128_warp(d_tmem, ptx::desc_lo(a_desc), ptx::desc_lo(b_desc), ptx::desc_hi(a_desc), C::kIdescS, 0u);
+  else
+    ptx::mma_ss_k64_warp(d_tmem, ptx::desc_lo(a_desc), ptx::desc_lo(b_desc), ptx::desc_hi(a_desc), C::kIdescS, 0u);
 }
 
 // Accumulating product over the 128 streamed rows: D[128 x HD] += A B with A
@@ -154,12 +154,9 @@ __device__ __forceinline__ void issue_tile_qk(uint32_t d_tmem, uint32_t a_tile, 
 template <int HD, int kHalf>
 __device__ __forceinline__ void issue_tile_acc(uint32_t d_tmem, uint32_t a_col, uint32_t b_tile, bool accumulate) {
   using C = BwdCfg<HD>;
-#pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    const uint64_t b_desc = ptx::desc_mnmajor_sw128(b_tile + kk * 16 * 128, C::kChunkBytes);
-    ptx::mma_ts_warp(d_tmem, a_col + kHalf * (kk >> 2) + 8 * (kk & 3), b_desc, C::kIdescAcc,
-                     (accumulate || kk > 0) ? 1u : 0u);
-  }
+  const uint64_t b_desc = ptx::desc_mnmajor_sw128(b_tile, C::kChunkBytes);
+  ptx::mma_ts_k128_warp<kHalf>(d_tmem, a_col, ptx::desc_lo(b_desc), ptx::desc_hi(b_desc), C::kIdescAcc,
+                               accumulate ? 1u : 0u);
 }
 
 // Epilogue helper: 32 accumulator columns of this thread's row, times `mul`,

@@ -208,23 +208,22 @@ __global__ void __launch_bounds__(DecCfg<HD>::kThreads, DecCfg<HD>::kCtasPerSm)
           if (!ok) break;
           ptx::tc_fence_after();
           const uint32_t v_tile = sKV + ((2 * (jj - 1) + 1) % C::kStages) * C::kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < C::kBN / 16; ++kk)
-            ptx::mma_ts_warp(tmem_base + C::kColO, tmem_base + C::kColS + kk * 8,
-                             ptx::desc_mnmajor_sw128(v_tile + kk * 16 * 128, C::kChunkBytes), C::kIdescPV,
-                             (jj > 1 || kk > 0) ? 1u : 0u);
+          const uint64_t b_desc = ptx::desc_mnmajor_sw128(v_tile, C::kChunkBytes);
+          ptx::mma_ts_k128_warp<32>(tmem_base + C::kColO, tmem_base + C::kColS, ptx::desc_lo(b_desc),
+                                    ptx::desc_hi(b_desc), C::kIdescPV, jj > 1 ? 1u : 0u);
           ptx::mma_commit_warp(ptx::smem_u32(&bar_kv_empty[(2 * (jj - 1) + 1) % C::kStages]));
         }
         ok = kv_wait(2 * jj);
         if (!ok) break;
         ptx::tc_fence_after();
         const uint32_t k_tile = sKV + ((2 * jj) % C::kStages) * C::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-          ptx::mma_ss_warp(tmem_base + C::kColS, ptx::desc_kmajor_sw128(sQ + off),
-                           ptx::desc_kmajor_sw128(k_tile + off), C::kIdescQK, kk > 0 ? 1u : 0u);
-        }
+        const uint64_t a_desc = ptx::desc_kmajor_sw128(sQ), b_desc = ptx::desc_kmajor_sw128(k_tile);
+        if constexpr (HD == 128)
+          ptx::mma_ss_k128_warp(tmem_base + C::kColS, ptx::desc_lo(a_desc), ptx::desc_lo(b_desc),
+                                ptx::desc_hi(a_desc), C::kIdescQK, 0u);
+        else
+          ptx::mma_ss_k64_warp(tmem_base + C::kColS, ptx::desc_lo(a_desc), ptx::desc_lo(b_desc),
+                               ptx::desc_hi(a_desc), C::kIdescQK, 0u);
         ptx::mma_commit_warp(ptx::smem_u32(&bar_s_full));
         ptx::mma_commit_warp(ptx::smem_u32(&bar_kv_empty[(2 * jj) % C::kStages]));
       }
@@ -235,11 +234,9 @@ __global__ void __launch_bounds__(DecCfg<HD>::kThreads, DecCfg<HD>::kCtasPerSm)
         if (ok) {
           ptx::tc_fence_after();
           const uint32_t v_tile = sKV + ((2 * (n - 1) + 1) % C::kStages) * C::kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < C::kBN / 16; ++kk)
-            ptx::mma_ts_warp(tmem_base + C::kColO, tmem_base + C::kColS + kk * 8,
-                             ptx::desc_mnmajor_sw128(v_tile + kk * 16 * 128, C::kChunkBytes), C::kIdescPV,
-                             (n > 1 || kk > 0) ? 1u : 0u);
+          const uint64_t b_desc = ptx::desc_mnmajor_sw128(v_tile, C::kChunkBytes);
+          ptx::mma_ts_k128_warp<32>(tmem_base + C::kColO, tmem_base + C::kColS, ptx::desc_lo(b_desc),
+                                    ptx::desc_hi(b_desc), C::kIdescPV, n > 1 ? 1u : 0u);
           ptx::mma_commit_warp(ptx::smem_u32(&bar_o_full));
           ptx::mma_commit_warp(ptx::smem_u32(&bar_kv_empty[(2 * (n - 1) + 1) % C::kStages]));
         }

@@ -268,11 +268,10 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
       const uint32_t v_tile = sKV + (it % C::kStages) * C::kTileBytes;
       const uint32_t d_tmem = tmem_base + C::kColO + HD * t;
       const uint32_t a_tmem = tmem_base + C::kColS + 128 * t;
-#pragma unroll
-      for (int kk = 0; kk < C::kBN / 16; ++kk) {
-        const uint64_t b_desc = ptx::desc_mnmajor_sw128(v_tile + kk * 16 * 128, C::kChunkBytes);
-        ptx::mma_ts_warp(d_tmem, a_tmem + kk * 8, b_desc, C::kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
-      }
+      static_assert(C::kBN == 128, "one burst of eight K = 16 products");
+      const uint64_t b_desc = ptx::desc_mnmajor_sw128(v_tile, C::kChunkBytes);
+      ptx::mma_ts_k128_warp<32>(d_tmem, a_tmem, ptx::desc_lo(b_desc), ptx::desc_hi(b_desc), C::kIdescPV,
+                                jj > 0 ? 1u : 0u);
     };
     // S_t = Q_t K_j^T.
     auto issue_qk = [&](int t, int j) {
@@ -280,12 +279,11 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
       const uint32_t k_tile = sKV + (it % C::kStages) * C::kTileBytes;
       const uint32_t q_tile = sQ + t * C::kTileBytes;
       const uint32_t d_tmem = tmem_base + C::kColS + 128 * t;
-#pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-        ptx::mma_ss_warp(d_tmem, ptx::desc_kmajor_sw128(q_tile + off), ptx::desc_kmajor_sw128(k_tile + off),
-                         C::kIdescQK, kk > 0 ? 1u : 0u);
-      }
+      const uint64_t a_desc = ptx::desc_kmajor_sw128(q_tile), b_desc = ptx::desc_kmajor_sw128(k_tile);
+      if constexpr (HD == 128)
+        ptx::mma_ss_k128_warp(d_tmem, ptx::desc_lo(a_desc), ptx::desc_lo(b_desc), ptx::desc_hi(a_desc), C::kIdescQK, 0u);
+      else
+        ptx::mma_ss_k64_warp(d_tmem, ptx::desc_lo(a_desc), ptx::desc_lo(b_desc), ptx::desc_hi(a_desc), C::kIdescQK, 0u);
     };
     // K_0 is waited for here; every later K_{j+1} and V_j is waited for by
     // the softmax warps before their hand-off for block j (p_full), so the

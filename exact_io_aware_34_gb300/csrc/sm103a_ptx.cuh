@@ -206,32 +206,74 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
-// The same two products issued from a converged warp: every lane calls them
-// and elect.sync picks one lane (lane 0 of a full warp) to issue. A single
+// Bursts of products issued from a converged warp: every lane calls these and
+// elect.sync picks one lane (lane 0 of a full warp) to issue. A single
 // diverged lane issues tcgen05.mma far more slowly than a converged warp when
 // other warps of its SM sub-partition compete for issue slots (measured on
 // GB300: 252 against 151 cycles per 128x128x16 product beside 8 busy warps).
-__device__ __forceinline__ void mma_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accum) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accum)
-      : "memory");
+// One asm block holds the group: one elect.sync and one accumulate predicate,
+// then per product only a 32-bit add on the descriptor's low word (its start
+// address in 16-byte units; the shared memory window is below 256 KB, so it
+// never carries into the next field) and the predicated tcgen05.mma. The
+// fewer instructions per product, the less of the issuing warp's share of
+// issue slots the group takes (1566 -> 1633 TFLOP/s on the 8k forward against
+// one asm statement per product). The first product accumulates when
+// acc0 != 0, the others always.
+#define FA_BURST_SS(OA) "add.u32 al, %1, " #OA ";\n\tadd.u32 bl, %2, " #OA ";\n\t" \
+  "mov.b64 ad, {al, %3};\n\tmov.b64 bd, {bl, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %4, t;\n\t"
+#define FA_BURST_SS_HEAD \
+  "{\n\t.reg .pred p, e, t;\n\t.reg .b32 al, bl;\n\t.reg .b64 ad, bd;\n\t" \
+  "setp.ne.b32 p, %5, 0;\n\tsetp.eq.u32 t, %4, %4;\n\telect.sync _|e, 0xffffffff;\n\t" \
+  "mov.b64 ad, {%1, %3};\n\tmov.b64 bd, {%2, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %4, p;\n\t"
+
+// K = 128 over two K-major 128-byte-swizzled chunks of 16 KB, A and B alike:
+// product kk starts at (kk / 4) * 16 KB + (kk % 4) * 32 B. a_lo / b_lo are the
+// low words of desc_kmajor_sw128 of the tiles, `hi` their (common) high word.
+__device__ __forceinline__ void mma_ss_k128_warp(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                                                 uint32_t idesc, uint32_t acc0) {
+  asm volatile(FA_BURST_SS_HEAD FA_BURST_SS(2) FA_BURST_SS(4) FA_BURST_SS(6) FA_BURST_SS(1024) FA_BURST_SS(1026)
+               FA_BURST_SS(1028) FA_BURST_SS(1030) "}" ::"r"(d_tmem),
+               "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(acc0)
+               : "memory");
 }
 
-__device__ __forceinline__ void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accum) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accum)
-      : "memory");
+// K = 64 within one chunk: product kk starts at kk * 32 B.
+__device__ __forceinline__ void mma_ss_k64_warp(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                                                uint32_t idesc, uint32_t acc0) {
+  asm volatile(FA_BURST_SS_HEAD FA_BURST_SS(2) FA_BURST_SS(4) FA_BURST_SS(6) "}" ::"r"(d_tmem), "r"(a_lo),
+               "r"(b_lo), "r"(hi), "r"(idesc), "r"(acc0)
+               : "memory");
 }
+
+// Eight products with A from TMEM and B MN-major over 128 rows of K (16 rows,
+// 2 KB, per product): B of product kk starts at kk * 2 KB; A at column
+// a_tmem + 8 * kk (kA4 = 32) or a_tmem + kA4 * (kk / 4) + 8 * (kk % 4).
+#define FA_BURST_TS(OA, OB) "add.u32 ta, %1, " #OA ";\n\tadd.u32 bl, %2, " #OB ";\n\t" \
+  "mov.b64 bd, {bl, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %4, t;\n\t"
+#define FA_BURST_TS_HEAD \
+  "{\n\t.reg .pred p, e, t;\n\t.reg .b32 ta, bl;\n\t.reg .b64 bd;\n\t" \
+  "setp.ne.b32 p, %5, 0;\n\tsetp.eq.u32 t, %4, %4;\n\telect.sync _|e, 0xffffffff;\n\t" \
+  "mov.b64 bd, {%2, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n\t"
+
+template <int kA4>
+__device__ __forceinline__ void mma_ts_k128_warp(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                                 uint32_t idesc, uint32_t acc0) {
+  static_assert(kA4 == 32 || kA4 == 64, "A column step per four products");
+  if constexpr (kA4 == 32) {
+    asm volatile(FA_BURST_TS_HEAD FA_BURST_TS(8, 128) FA_BURST_TS(16, 256) FA_BURST_TS(24, 384)
+                 FA_BURST_TS(32, 512) FA_BURST_TS(40, 640) FA_BURST_TS(48, 768) FA_BURST_TS(56, 896) "}" ::"r"(d_tmem),
+                 "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc0)
+                 : "memory");
+  } else {
+    asm volatile(FA_BURST_TS_HEAD FA_BURST_TS(8, 128) FA_BURST_TS(16, 256) FA_BURST_TS(24, 384)
+                 FA_BURST_TS(64, 512) FA_BURST_TS(72, 640) FA_BURST_TS(80, 768) FA_BURST_TS(88, 896) "}" ::"r"(d_tmem),
+                 "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc0)
+                 : "memory");
+  }
+}
+
+__device__ __forceinline__ uint32_t desc_lo(uint64_t d) { return static_cast<uint32_t>(d); }
+__device__ __forceinline__ uint32_t desc_hi(uint64_t d) { return static_cast<uint32_t>(d >> 32); }
 
 // mma_commit from a converged warp: the elected lane (the one that issued the
 // products above) arrives.
