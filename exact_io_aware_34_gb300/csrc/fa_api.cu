@@ -318,6 +318,148 @@ fa_status_t bwd_launch(const void* Q, const void* K, const void* V, const void* 
   return FA_OK;
 }
 
+// ---------------------------------------------------------------- host buffers
+// fa_fwd_host: the device copies of Q, K, V, O and LSE live in the caller's
+// workspace, each part 256-byte aligned.
+constexpr int kHostMaxChunks = 16;
+
+size_t align256(size_t n) { return (n + 255) / 256 * 256; }
+
+size_t host_workspace_bytes(int B, int H, int N, int d) {
+  const size_t n_qkv = static_cast<size_t>(B) * H * N * d * 2;
+  const size_t n_lse = static_cast<size_t>(B) * H * N * 4;
+  return 4 * align256(n_qkv) + align256(n_lse);
+}
+
+// Streams and events of the host path, one set per device, created on first
+// use and kept for the life of the process: an upload stream, a download
+// stream, and a second compute stream so that consecutive chunk kernels may
+// overlap. Calls are serialised by `mu` while they enqueue, which lets them
+// reuse the events: a stream wait takes the event's state when it is enqueued.
+struct HostPath {
+  std::mutex mu;
+  cudaStream_t up = nullptr, down = nullptr, aux = nullptr;
+  cudaEvent_t start = nullptr, end = nullptr;
+  cudaEvent_t in[kHostMaxChunks] = {}, done[kHostMaxChunks] = {};
+  cudaError_t err = cudaSuccess;
+};
+
+HostPath* host_path(int dev) {
+  static HostPath hp[64];
+  static std::once_flag once[64];
+  std::call_once(once[dev], [dev] {
+    HostPath& h = hp[dev];
+    cudaError_t e = cudaStreamCreateWithFlags(&h.up, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h.down, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h.aux, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.start, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.end, cudaEventDisableTiming);
+    for (int c = 0; c < kHostMaxChunks && e == cudaSuccess; ++c) {
+      e = cudaEventCreateWithFlags(&h.in[c], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.done[c], cudaEventDisableTiming);
+    }
+    h.err = e;
+  });
+  return &hp[dev];
+}
+
+// Heads per chunk: about 8 chunks, so that the first upload and the last
+// download, which nothing overlaps, are short.
+int host_chunks(int BH, int num_chunks) {
+  const int nc = num_chunks > 0 ? num_chunks : 8;
+  return std::max(1, std::min({nc, BH, kHostMaxChunks}));
+}
+
+fa_status_t host_impl(const void* Qh, const void* Kh, const void* Vh, void* Oh, float* LSEh, int B, int H, int N,
+                      int d, float scale, int num_chunks, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream) {
+  if (!Qh || !Kh || !Vh || !Oh || !LSEh) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1 || d < 1 || num_chunks < 0) return FA_ERR_INVALID_ARG;
+  if (B > 65535 || H > 65535) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H * N >= (1LL << 31)) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (scale < 0.f) return FA_ERR_UNSUPPORTED;
+  const size_t need = host_workspace_bytes(B, H, N, d);
+  if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256 != 0 || workspace_bytes < need)
+    return FA_ERR_INVALID_ARG;
+  const size_t n_qkv = static_cast<size_t>(B) * H * N * d * 2;
+  const size_t n_lse = static_cast<size_t>(B) * H * N * 4;
+  for (const void* a : {Qh, Kh, Vh}) {
+    if (overlaps(Oh, n_qkv, a, n_qkv) || overlaps(LSEh, n_lse, a, n_qkv)) return FA_ERR_INVALID_ARG;
+  }
+  if (overlaps(Oh, n_qkv, LSEh, n_lse)) return FA_ERR_INVALID_ARG;
+  for (const void* a : {Qh, Kh, Vh, static_cast<const void*>(Oh), static_cast<const void*>(LSEh)})
+    if (overlaps(a, a == LSEh ? n_lse : n_qkv, workspace, need)) return FA_ERR_INVALID_ARG;
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= 64) return FA_ERR_UNSUPPORTED;
+  HostPath* hp = host_path(dev);
+  if (hp->err != cudaSuccess) return cuda_fail(hp->err);
+
+  char* Qd = static_cast<char*>(workspace);
+  char* Kd = Qd + align256(n_qkv);
+  char* Vd = Kd + align256(n_qkv);
+  char* Od = Vd + align256(n_qkv);
+  char* Ld = Od + align256(n_qkv);
+  const char* qh = static_cast<const char*>(Qh);
+  const char* kh = static_cast<const char*>(Kh);
+  const char* vh = static_cast<const char*>(Vh);
+  char* oh = static_cast<char*>(Oh);
+  char* lh = reinterpret_cast<char*>(LSEh);
+
+  const int BH = B * H;
+  const int nc = host_chunks(BH, num_chunks);
+  const int per = (BH + nc - 1) / nc;
+  const size_t head_bytes = static_cast<size_t>(N) * d * 2;
+  const size_t head_lse = static_cast<size_t>(N) * 4;
+
+  std::lock_guard<std::mutex> lock(hp->mu);
+#define FA_TRY(x)                              \
+  do {                                         \
+    cudaError_t e_ = (x);                      \
+    if (e_ != cudaSuccess) return cuda_fail(e_); \
+  } while (0)
+  // Everything below runs after the work already on `stream` (which may still
+  // use the workspace), and `stream` resumes only after the last download.
+  FA_TRY(cudaEventRecord(hp->start, stream));
+  FA_TRY(cudaStreamWaitEvent(hp->up, hp->start, 0));
+  FA_TRY(cudaStreamWaitEvent(hp->aux, hp->start, 0));
+  FA_TRY(cudaStreamWaitEvent(hp->down, hp->start, 0));
+  for (int c = 0; c < nc; ++c) {
+    const int bh0 = c * per;
+    const int nbh = std::min(per, BH - bh0);
+    if (nbh <= 0) break;
+    const size_t off = static_cast<size_t>(bh0) * head_bytes, bytes = static_cast<size_t>(nbh) * head_bytes;
+    const size_t loff = static_cast<size_t>(bh0) * head_lse, lbytes = static_cast<size_t>(nbh) * head_lse;
+    FA_TRY(cudaMemcpyAsync(Qd + off, qh + off, bytes, cudaMemcpyHostToDevice, hp->up));
+    FA_TRY(cudaMemcpyAsync(Kd + off, kh + off, bytes, cudaMemcpyHostToDevice, hp->up));
+    FA_TRY(cudaMemcpyAsync(Vd + off, vh + off, bytes, cudaMemcpyHostToDevice, hp->up));
+    FA_TRY(cudaEventRecord(hp->in[c], hp->up));
+    cudaStream_t cs = (c & 1) ? hp->aux : stream;
+    FA_TRY(cudaStreamWaitEvent(cs, hp->in[c], 0));
+    // The chunk's heads as a [1, nbh, N, d] problem: the same kernel and the
+    // same per-head result as fa_fwd.
+    const fa_status_t st =
+        d == 64 ? launch<64>(Qd + off, Kd + off, Vd + off, Od + off, reinterpret_cast<float*>(Ld + loff), 1, nbh,
+                             nbh, N, N, scale, -1, kDefaultTimeoutNs, cs)
+                : launch<128>(Qd + off, Kd + off, Vd + off, Od + off, reinterpret_cast<float*>(Ld + loff), 1, nbh,
+                              nbh, N, N, scale, -1, kDefaultTimeoutNs, cs);
+    if (st != FA_OK) return st;
+    FA_TRY(cudaEventRecord(hp->done[c], cs));
+    FA_TRY(cudaStreamWaitEvent(hp->down, hp->done[c], 0));
+    FA_TRY(cudaMemcpyAsync(oh + off, Od + off, bytes, cudaMemcpyDeviceToHost, hp->down));
+    FA_TRY(cudaMemcpyAsync(lh + loff, Ld + loff, lbytes, cudaMemcpyDeviceToHost, hp->down));
+  }
+  // The downloads follow every chunk's kernel, so the last one covers all.
+  FA_TRY(cudaEventRecord(hp->end, hp->down));
+  FA_TRY(cudaStreamWaitEvent(stream, hp->end, 0));
+#undef FA_TRY
+  return FA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -325,6 +467,17 @@ extern "C" {
 fa_status_t fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
                    float scale, cudaStream_t stream) {
   return fwd_impl(Q, K, V, O, LSE, B, H, N, d, scale, -1, kDefaultTimeoutNs, stream);
+}
+
+size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+  return host_workspace_bytes(B, H, N, d);
+}
+
+fa_status_t fa_fwd_host(const void* Qh, const void* Kh, const void* Vh, void* Oh, float* LSEh, int B, int H, int N,
+                        int d, float scale, int num_chunks, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream) {
+  return host_impl(Qh, Kh, Vh, Oh, LSEh, B, H, N, d, scale, num_chunks, workspace, workspace_bytes, stream);
 }
 
 fa_status_t fa_fwd_fault_test(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,

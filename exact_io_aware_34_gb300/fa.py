@@ -27,7 +27,7 @@ FA_ERR_TIMEOUT = 4
 EXPORTED = ("fa_fwd", "fa_get_device_status", "fa_status_string", "fa_last_cuda_error", "fa_fwd_fault_test",
             "fa_naive_fwd", "fa_naive_workspace_bytes", "fa_naive_fwd_noalloc", "fa_bwd", "fa_bwd_workspace_bytes",
             "fa_bwd_fault_test", "fa_fwd_kv", "fa_fwd_kv_num_splits", "fa_fwd_kv_workspace_bytes",
-            "fa_fwd_kv_fault_test", "fa_merge_partials")
+            "fa_fwd_kv_fault_test", "fa_merge_partials", "fa_fwd_host", "fa_fwd_host_workspace_bytes")
 
 _lib = None
 
@@ -52,6 +52,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     vp, i, f, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_ulonglong
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, vp]
     lib.fa_fwd.restype = i
+    lib.fa_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, ctypes.c_size_t, vp]
+    lib.fa_fwd_host.restype = i
+    lib.fa_fwd_host_workspace_bytes.argtypes = [i, i, i, i]
+    lib.fa_fwd_host_workspace_bytes.restype = ctypes.c_size_t
     lib.fa_fwd_fault_test.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, u64, vp]
     lib.fa_fwd_fault_test.restype = i
     lib.fa_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
@@ -148,6 +152,55 @@ def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor | 
     if st != FA_OK:
         raise FaError(st, "fa_fwd")
     return o, lse
+
+
+def fa_fwd_host_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(load_library().fa_fwd_host_workspace_bytes(int(B), int(H), int(N), int(d)))
+
+
+def fa_fwd_host(qh: torch.Tensor, kh: torch.Tensor, vh: torch.Tensor, oh: torch.Tensor | None = None,
+                lseh: torch.Tensor | None = None, scale: float | None = None, num_chunks: int = 0, workspace=None,
+                device=None, stream=None):
+    """fa_fwd on host tensors, end to end (upload, kernel, download, pipelined
+    over head groups by the library).
+
+    qh, kh, vh: bf16 CPU tensors [B, H, N, d], contiguous (pinned for full copy
+    bandwidth). ``oh`` / ``lseh`` (CPU, allocated pinned when not given) receive
+    O and LSE. ``workspace``: a CUDA uint8 tensor of at least
+    fa_fwd_host_workspace_bytes(B, H, N, d) bytes on ``device`` (default: the
+    current CUDA device), allocated with torch when None. The call is
+    asynchronous on ``stream``: synchronise it before reading ``oh`` and
+    ``lseh``. Returns (oh, lseh).
+    """
+    for x in (qh, kh, vh):
+        if x.device.type != "cpu" or x.dtype != torch.bfloat16 or not x.is_contiguous() or x.dim() != 4:
+            raise ValueError("qh, kh, vh must be contiguous bf16 CPU tensors [B, H, N, d]")
+    if not (qh.shape == kh.shape == vh.shape):
+        raise ValueError("qh, kh, vh must have the same shape")
+    B, H, N, d = qh.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if oh is None:
+        oh = torch.empty(qh.shape, dtype=torch.bfloat16).pin_memory()
+    if lseh is None:
+        lseh = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    if oh.device.type != "cpu" or oh.dtype != torch.bfloat16 or oh.shape != qh.shape or not oh.is_contiguous():
+        raise ValueError("oh must be a contiguous bf16 CPU tensor shaped like qh")
+    if lseh.device.type != "cpu" or lseh.dtype != torch.float32 or tuple(lseh.shape) != (B, H, N) \
+            or not lseh.is_contiguous():
+        raise ValueError("lseh must be a contiguous float32 CPU tensor [B, H, N]")
+    need = fa_fwd_host_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    lib = load_library()
+    with torch.cuda.device(dev):
+        st = lib.fa_fwd_host(qh.data_ptr(), kh.data_ptr(), vh.data_ptr(), oh.data_ptr(), lseh.data_ptr(), B, H, N, d,
+                             float(scale), int(num_chunks), workspace.data_ptr(),
+                             workspace.numel() * workspace.element_size(), _stream_handle(stream, dev))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_host")
+    return oh, lseh
 
 
 def fa_naive_workspace_bytes(B: int, H: int, N: int) -> int:

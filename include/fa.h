@@ -74,6 +74,38 @@ fa_status_t fa_fwd(const void* Q, const void* K, const void* V, void* O, float* 
                    int B, int H, int N, int d, float scale, cudaStream_t stream);
 
 /*
+ * fa_fwd_host_workspace_bytes -- device workspace fa_fwd_host needs: room for
+ * device copies of Q, K, V, O (bf16 [B, H, N, d] each) and LSE (float32
+ * [B, H, N]), each part padded to 256 bytes. 0 for unsupported sizes.
+ */
+size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * fa_fwd_host -- fa_fwd on HOST buffers, end to end: uploads Q, K, V, runs the
+ * forward kernel and downloads O and LSE, pipelined over groups of (b, h)
+ * heads so that the uploads of one group and the downloads of another overlap
+ * the kernel on a third. Each head's O and LSE are bit for bit those of fa_fwd.
+ *   Qh, Kh, Vh : host, bf16 [B, H, N, d], read. Page-locked (pinned) memory
+ *                gives full copy bandwidth; pageable memory works, slower.
+ *   Oh, LSEh   : host, bf16 [B, H, N, d] and float32 [B, H, N], written.
+ *   num_chunks : head groups (0 = automatic: 8, at most B*H and 16).
+ *   workspace  : device, fa_fwd_host_workspace_bytes(B, H, N, d) bytes at
+ *                least, 256-byte aligned, owned by the caller, overlapping no
+ *                host buffer; its contents are overwritten.
+ *   stream     : the call is ordered after the work already on `stream`, and
+ *                `stream` reaches the end of the call only when Oh and LSEh
+ *                are written: synchronise `stream` before reading them. The
+ *                copies run on two internal streams and every second group's
+ *                kernel on a third (created once per device).
+ * Limits and error codes as for fa_fwd, checked on the host before anything
+ * is enqueued; FA_ERR_INVALID_ARG also for a missing, misaligned, small or
+ * overlapping workspace or overlapping host buffers.
+ */
+fa_status_t fa_fwd_host(const void* Qh, const void* Kh, const void* Vh, void* Oh, float* LSEh,
+                        int B, int H, int N, int d, float scale, int num_chunks,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * fa_get_device_status -- synchronise `stream`, then read and clear the
  * library's device status word on the current device. Returns FA_OK, or
  * FA_ERR_TIMEOUT if any kernel of this library on this device gave up on a

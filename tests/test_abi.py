@@ -240,3 +240,40 @@ def test_merge_host_side_rejections(lib, kwargs, expect):
     args.update(kwargs)
     assert lib.fa_merge_partials(args["Op"], args["Lp"], args["O"], args["L"], args["P"], args["rows"], args["d"],
                                  None) == expect
+
+
+# --- host-buffer forward (fa_fwd_host): checks that fail before any CUDA call -----------
+def host_call(lib, **kw):
+    args = dict(Q=A, K=A + GAP, V=A + 2 * GAP, O=A + 3 * GAP, L=A + 4 * GAP, B=1, H=4, N=1000, d=128, scale=0.1,
+                chunks=0, ws=A + 5 * GAP, ws_bytes=1 << 40)
+    args.update(kw)
+    return lib.fa_fwd_host(args["Q"], args["K"], args["V"], args["O"], args["L"], args["B"], args["H"], args["N"],
+                           args["d"], ctypes.c_float(args["scale"]), args["chunks"], args["ws"], args["ws_bytes"], None)
+
+
+def test_host_workspace_bytes(lib):
+    pad = lambda n: (n + 255) // 256 * 256
+    assert fa.fa_fwd_host_workspace_bytes(1, 4, 1000, 128) == 4 * pad(4 * 1000 * 128 * 2) + pad(4 * 1000 * 4)
+    assert fa.fa_fwd_host_workspace_bytes(2, 3, 77, 64) == 4 * pad(6 * 77 * 64 * 2) + pad(6 * 77 * 4)
+    assert fa.fa_fwd_host_workspace_bytes(1, 4, 1000, 96) == 0
+    assert fa.fa_fwd_host_workspace_bytes(0, 4, 1000, 128) == 0
+
+
+@pytest.mark.parametrize("kwargs,expect", [
+    (dict(Q=0), fa.FA_ERR_INVALID_ARG),
+    (dict(O=0), fa.FA_ERR_INVALID_ARG),
+    (dict(L=0), fa.FA_ERR_INVALID_ARG),
+    (dict(N=0), fa.FA_ERR_INVALID_ARG),
+    (dict(chunks=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(scale=-1.0), fa.FA_ERR_UNSUPPORTED),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(ws=0), fa.FA_ERR_INVALID_ARG),                                   # no workspace
+    (dict(ws=A + 5 * GAP + 128), fa.FA_ERR_INVALID_ARG),                   # not 256-byte aligned
+    (dict(ws_bytes=4 * 4 * 1000 * 256 + 16000 - 1), fa.FA_ERR_INVALID_ARG),  # too small
+    (dict(O=A + 64), fa.FA_ERR_INVALID_ARG),                                # O overlaps Q
+    (dict(L=A + 3 * GAP + 8), fa.FA_ERR_INVALID_ARG),                       # LSE overlaps O
+    (dict(ws=A + 2 * GAP), fa.FA_ERR_INVALID_ARG),                          # workspace overlaps V
+])
+def test_host_side_rejections_host_path(lib, kwargs, expect):
+    assert host_call(lib, **kwargs) == expect
