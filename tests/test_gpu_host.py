@@ -79,3 +79,14 @@ def test_host_path_rejects_device_tensors():
     q, k, v = inputs.make_random(1, 1, 128, 64, seed=5)
     with pytest.raises(ValueError):
         fa.fa_fwd_host(q.cuda(), k, v)
+
+
+def test_pageable_host_buffers():
+    """Unpinned host memory: slower copies, the same result."""
+    q, k, v = inputs.make_random(1, 3, 333, 64, seed=81)
+    oh, lh = fa.fa_fwd_host(q.contiguous(), k.contiguous(), v.contiguous(), scale=0.125, num_chunks=2,
+                            oh=torch.empty(q.shape, dtype=torch.bfloat16), lseh=torch.empty((1, 3, 333)))
+    torch.cuda.synchronize()
+    od, ld = parity.run_gpu(q, k, v, 0.125)
+    assert bits_equal(oh, od)
+    assert torch.equal(lh, ld)
