@@ -743,9 +743,21 @@ fa_status_t decode_launch(const void* Q, const void* K, const void* V, void* O, 
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   if (k.num_splits > 1) {
-    fa::decode_merge_kernel<HD><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
-        p.O_part, p.LSE_part, static_cast<__nv_bfloat16*>(O), LSE, static_cast<long long>(rows), k.num_splits);
-    e = cudaGetLastError();
+    // The merge as a programmatic dependent launch: it is scheduled while the
+    // decode grid finishes and waits (griddepcontrol.wait) for its partials.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((rows + 7) / 8));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, fa::decode_merge_kernel<HD>, static_cast<const float*>(p.O_part),
+                           static_cast<const float*>(p.LSE_part), static_cast<__nv_bfloat16*>(O), LSE,
+                           static_cast<long long>(rows), k.num_splits);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   return FA_OK;

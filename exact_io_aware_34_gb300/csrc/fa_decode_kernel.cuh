@@ -391,6 +391,8 @@ __global__ void __launch_bounds__(DecCfg<HD>::kThreads, DecCfg<HD>::kCtasPerSm)
     }
   }
 
+  // The merge kernel may be scheduled now; it waits for this grid's end.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 5) {
@@ -401,29 +403,48 @@ __global__ void __launch_bounds__(DecCfg<HD>::kThreads, DecCfg<HD>::kCtasPerSm)
 
 // One warp per query row: combine the num_splits partial results of the row.
 // LSE = m + ln sum_s e^{LSE_s - m} with m = max_s LSE_s, and
-// O = sum_s e^{LSE_s - LSE} O_s, rounded once to bf16.
+// O = sum_s e^{LSE_s - LSE} O_s, rounded once to bf16. The splits' LSE are
+// read by the lanes in parallel (32 at a time) and their weights passed by
+// shuffles, so the row costs two dependent rounds of loads, not 2 x splits.
 template <int HD>
 __global__ void __launch_bounds__(256) decode_merge_kernel(const float* __restrict__ O_part,
                                                            const float* __restrict__ LSE_part,
                                                            __nv_bfloat16* __restrict__ O, float* __restrict__ LSE,
                                                            long long n_rows, int num_splits) {
+  // Launched as a programmatic dependent of the decode kernel: wait here until
+  // that grid has finished and its partials are visible (returns at once when
+  // there is no such grid).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (row >= n_rows) return;
   float m = -INFINITY;
-  for (int s = 0; s < num_splits; ++s) m = fmaxf(m, LSE_part[s * n_rows + row]);
+  for (int s0 = 0; s0 < num_splits; s0 += 32) {
+    const int s = s0 + lane;
+    if (s < num_splits) m = fmaxf(m, LSE_part[s * n_rows + row]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   constexpr int kPer = HD / 32;     // output elements per lane: 4 or 2
   float acc[kPer];
 #pragma unroll
   for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
   float total = 0.f;
-  for (int s = 0; s < num_splits; ++s) {
-    const float w = __expf(LSE_part[s * n_rows + row] - m);
-    total += w;
-    const float* src = O_part + (s * n_rows + row) * HD + lane * kPer;
+  for (int s0 = 0; s0 < num_splits; s0 += 32) {
+    const int s_me = s0 + lane;
+    const float w_me = s_me < num_splits ? __expf(LSE_part[s_me * n_rows + row] - m) : 0.f;
+    total += w_me;
+    const int cnt = min(32, num_splits - s0);
+#pragma unroll 4
+    for (int i = 0; i < cnt; ++i) {
+      const float w = __shfl_sync(0xffffffffu, w_me, i);
+      const float* src = O_part + ((s0 + i) * n_rows + row) * HD + lane * kPer;
 #pragma unroll
-    for (int e = 0; e < kPer; ++e) acc[e] = fmaf(w, src[e], acc[e]);
+      for (int e = 0; e < kPer; ++e) acc[e] = fmaf(w, src[e], acc[e]);
+    }
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
   const float inv = 1.f / total;
   __nv_bfloat16* dst = O + row * HD + lane * kPer;
 #pragma unroll

@@ -202,7 +202,8 @@ fa_status_t fa_naive_fwd_noalloc(const void* Q, const void* K, const void* V, vo
  * the heads sharing a K/V head are packed into one tile (min(H/H_kv, 128/N_q)
  * heads per tile), so each K/V tile is read once per group; for N_q > 128 a
  * tile is one 128-row block of one head. Launches: one kernel, plus one merge
- * kernel when there is more than one split. Limits as for fa_fwd;
+ * kernel when there is more than one split (a programmatic dependent launch:
+ * it is scheduled as the first grid ends and waits for it on the device). Limits as for fa_fwd;
  * FA_ERR_INVALID_ARG also when H is not a multiple of H_kv or for a missing,
  * misaligned, small or overlapping workspace.
  */
