@@ -36,7 +36,8 @@
 //              w & 3 (32 rows) and the 64 streamed-block columns
 //              [64 (w >> 2), 64 (w >> 2) + 64)
 //   warp 8     TMA producer (one thread)
-//   warp 9     TMEM allocator and MMA issuer (one thread)
+//   warp 9     TMEM allocator and MMA issuer (the whole warp, converged; one
+//              elected lane issues each tcgen05 instruction)
 // Packed bf16 results of warp half h live in that half's own score columns
 // [64h, 64h + 32) (and dS of the key-block kernel in [64h + 32, 64h + 64)),
 // so that no warp overwrites scores another warp has yet to load. For the

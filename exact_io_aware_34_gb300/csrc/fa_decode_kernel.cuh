@@ -24,7 +24,8 @@
 //
 // Per CTA (192 threads): warps 0-3 run the softmax and epilogue of the one
 // tile (one thread per row), warp 4 is the TMA producer, warp 5 allocates
-// TMEM and issues the MMAs. TMEM: S at column 0 (P, packed bf16, over its
+// TMEM and issues the MMAs (converged, one elected lane issuing). TMEM: S at
+// column 0 (P, packed bf16, over its
 // first 64 columns), O at column 128. The per-block update is the forward
 // kernel's, including the lazy rescale. With a single tile, a CTA's QK^T,
 // softmax and PV of a block run one after another; two CTAs per SM (a

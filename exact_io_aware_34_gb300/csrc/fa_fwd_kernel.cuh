@@ -29,7 +29,8 @@
 //   warps 0-3  softmax + epilogue for query tile 0 (one thread per row)
 //   warps 4-7  softmax + epilogue for query tile 1
 //   warp 8     TMA producer (one thread)
-//   warp 9     TMEM allocator and MMA issuer (one thread issues)
+//   warp 9     TMEM allocator and MMA issuer (the whole warp, converged; one
+//              elected lane issues each tcgen05 instruction)
 // TMEM (512 columns x 128 lanes x 32 bit): S_t at column 128*t (P_t, packed
 // bf16, overwrites the first 64 of those columns), O_t at 256 + d*t.
 // Shared memory: Q tiles (2 x 128 x d bf16) + a ring of K/V tiles
