@@ -90,3 +90,15 @@ def test_pageable_host_buffers():
     od, ld = parity.run_gpu(q, k, v, 0.125)
     assert bits_equal(oh, od)
     assert torch.equal(lh, ld)
+
+
+def test_full_workload_in_the_bench_configuration():
+    """prefill8k_d128_h32 through fa_fwd_host with the automatic head groups, as the bench's e2e
+    times it: bit for bit fa_fwd's result (which the full-size parity tests check against the
+    oracle on sampled rows)."""
+    w = inputs.workload("prefill8k_d128_h32")
+    q, k, v, scale = inputs.make_inputs(w)
+    oh, lh = run_host(q, k, v, scale)
+    od, ld = parity.run_gpu(q, k, v, scale)
+    assert bits_equal(oh, od)
+    assert torch.equal(lh, ld)
