@@ -322,14 +322,14 @@ __global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
     {
       auto k_tile = [&](int j) { return sK + (j % D::kKSlots) * C::kTileBytes; };
       auto v_tile = [&](int j) { return sV + (j % D::kVSlots) * C::kTileBytes; };
-      // S_j = Q K_j^T and dP_j = dO V_j^T, after K_j and V_j have landed.
+      // S_j = Q K_j^T and dP_j = dO V_j^T. K_0 and V_0 are waited for here;
+      // every later K_{j+1} and V_{j+1} by the elementwise warps before their
+      // dp_free(j), so that this warp waits only on the hand-offs.
       auto issue_sdp = [&](int j) -> bool {
-        if (!wait_warp_or_abort(ptx::smem_u32(&bar_k_full[j % D::kKSlots]), (j / D::kKSlots) & 1, abort_ptr,
-                           p.timeout_ns, kRoleDqMma))
-          return false;
-        if (!wait_warp_or_abort(ptx::smem_u32(&bar_v_full[j % D::kVSlots]), (j / D::kVSlots) & 1, abort_ptr,
-                           p.timeout_ns, kRoleDqMma))
-          return false;
+        if (j == 0) {
+          if (!wait_warp_or_abort(ptx::smem_u32(&bar_k_full[0]), 0, abort_ptr, p.timeout_ns, kRoleDqMma)) return false;
+          if (!wait_warp_or_abort(ptx::smem_u32(&bar_v_full[0]), 0, abort_ptr, p.timeout_ns, kRoleDqMma)) return false;
+        }
         ptx::tc_fence_after();
         issue_tile_qk<HD>(tmem_base + D::kColS, sQ, k_tile(j));
         issue_tile_qk<HD>(tmem_base + D::kColP, sdO, v_tile(j));
@@ -389,6 +389,16 @@ __global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
       ptx::reg_fence32(s[1]);
       ptx::reg_fence32(dp[0]);
       ptx::reg_fence32(dp[1]);
+      if (j + 1 < n) {
+        // K_{j+1} and V_{j+1} in place before the hand-off that lets S/dP of
+        // block j+1 be issued.
+        ok = wait_warp_or_abort(ptx::smem_u32(&bar_k_full[(j + 1) % D::kKSlots]), ((j + 1) / D::kKSlots) & 1,
+                                abort_ptr, p.timeout_ns, kRoleDqSoftmax);
+        if (ok)
+          ok = wait_warp_or_abort(ptx::smem_u32(&bar_v_full[(j + 1) % D::kVSlots]), ((j + 1) / D::kVSlots) & 1,
+                                  abort_ptr, p.timeout_ns, kRoleDqSoftmax);
+        if (!ok) break;
+      }
       ptx::tc_fence_before();
       ptx::mbar_arrive(ptx::smem_u32(&bar_dp_free));
 
