@@ -575,15 +575,21 @@ __global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
         ptx::mma_commit_warp(ptx::smem_u32(&bar_s_full));
       }
       for (int i = 0; i < n && ok; ++i) {
+        // S_{i+1}^T goes in as soon as region(i+1) is free (dp_free(i)) if the
+        // (Q, dO) pair of block i+1 has already landed; a late pair must not
+        // hold back dV/dK(i), whose commit frees the ring slot the next copy
+        // needs.
+        bool s_issued = false;
+        const int s1 = (i + 1) % C::kStages;
+        const uint32_t in_par = ((i + 1) / C::kStages) & 1;
         if (i + 1 < n) {
-          const int s1 = (i + 1) % C::kStages;
-          ok = wait_warp_or_abort(ptx::smem_u32(&bar_in_full[s1]), ((i + 1) / C::kStages) & 1, abort_ptr, p.timeout_ns,
-                             kRoleDkvMma);
-          if (!ok) break;
           ok = wait_warp_or_abort(ptx::smem_u32(&bar_dp_free), i & 1, abort_ptr, p.timeout_ns, kRoleDkvMma);
           if (!ok) break;
-          ptx::tc_fence_after();
-          issue_tile_qk<HD>(region(i + 1), sK, q_tile(i + 1));          // S_{i+1}^T
+          if (__all_sync(0xffffffffu, ptx::mbar_test_wait(ptx::smem_u32(&bar_in_full[s1]), in_par))) {
+            ptx::tc_fence_after();
+            issue_tile_qk<HD>(region(i + 1), sK, q_tile(i + 1));        // S_{i+1}^T
+            s_issued = true;
+          }
         }
         ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_full), i & 1, abort_ptr, p.timeout_ns, kRoleDkvMma);
         if (!ok) break;
@@ -592,6 +598,12 @@ __global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
         issue_tile_acc<HD, 64>(tmem_base + kColDK, region(i) + 32, q_tile(i), i > 0);             // dK += dS^T Q_i
         ptx::mma_commit_warp(ptx::smem_u32(&bar_in_empty[i % C::kStages]));
         if (i + 1 < n) {
+          if (!s_issued) {
+            ok = wait_warp_or_abort(ptx::smem_u32(&bar_in_full[s1]), in_par, abort_ptr, p.timeout_ns, kRoleDkvMma);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            issue_tile_qk<HD>(region(i + 1), sK, q_tile(i + 1));        // S_{i+1}^T
+          }
           issue_tile_qk<HD>(region(i), sV, q_tile(i + 1) + C::kTileBytes);   // dP_{i+1}^T
           ptx::mma_commit_warp(ptx::smem_u32(&bar_s_full));
         }
