@@ -88,7 +88,7 @@ size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d);
  *   Qh, Kh, Vh : host, bf16 [B, H, N, d], read. Page-locked (pinned) memory
  *                gives full copy bandwidth; pageable memory works, slower.
  *   Oh, LSEh   : host, bf16 [B, H, N, d] and float32 [B, H, N], written.
- *   num_chunks : head groups (0 = automatic: 8, at most B*H and 16).
+ *   num_chunks : head groups, 0 for the default of 8; capped at B*H and at 16.
  *   workspace  : device, fa_fwd_host_workspace_bytes(B, H, N, d) bytes at
  *                least, 256-byte aligned, owned by the caller, overlapping no
  *                host buffer; its contents are overwritten.
