@@ -406,6 +406,24 @@ def cpu_baseline(name: str, target_s: float = 15.0):
                       f"float64 numpy oracle, {t.cores} single-threaded worker processes, {dt:.1f} s"}
 
 
+# The small configurations also timed on one host core (the whole workload, or
+# as much of it as about `target_s` seconds allows).
+SMALL_WORKLOADS = ("n256_d64", "n1024_d64_b4h16")
+
+
+def cpu_baseline_single_core(name: str, target_s: float = 2.0):
+    t = OracleTimer(name, cores=1)
+    try:
+        rows = t.calibrate(target_s)
+        dt, flops = t.run(rows, seed=1)
+    finally:
+        t.close()
+    total = t.w.B * t.w.H * t.w.N
+    return {"workload": name, "value": flops / dt / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{rows} of the {total} query rows of {name} (all {t.w.N} keys each), float64 numpy oracle, "
+                      f"one single-threaded worker process, {dt:.2f} s"}
+
+
 # ----------------------------------------------------------------------------- reference arm
 def run_reference(args):
     world, rank, _ = dist_setup()
@@ -455,8 +473,10 @@ def run_native(args):
 
     # The CPU baseline runs before the first GPU call (its worker pool is spawned).
     cpu = cpu_bwd = cpu_dec = None
+    cpu_small = []
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.workload, target_s=args.cpu_seconds)
+        cpu_small = [cpu_baseline_single_core(n) for n in SMALL_WORKLOADS]
         if not args.no_bwd:
             cpu_bwd = cpu_baseline_bwd(args.workload, target_s=min(10.0, args.cpu_seconds))
         if not args.no_decode:
@@ -699,6 +719,8 @@ def run_native(args):
             line["decode"] = decode
         if cpu is not None:
             line["cpu_baseline"] = cpu
+        if cpu_small:
+            line["cpu_baseline_1core"] = cpu_small
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -92,3 +92,11 @@ def test_cpu_baselines_of_the_next_rows():
     assert rb["kind"] == "oracle" and rb["unit"] == "TFLOP/s" and rb["value"] > 0 and rb["cores"] >= 1
     rd = bench.cpu_baseline_decode("decode32k_gqa8_b4")
     assert rd["kind"] == "oracle" and rd["unit"] == "GB/s" and rd["value"] > 0
+
+
+def test_cpu_baseline_single_core():
+    """The one-core oracle timing of a small configuration is a well-formed record."""
+    import bench
+    r = bench.cpu_baseline_single_core("n256_d64", target_s=0.2)
+    assert r["kind"] == "oracle" and r["cores"] == 1 and r["unit"] == "TFLOP/s" and r["value"] > 0
+    assert r["workload"] == "n256_d64"
