@@ -102,3 +102,40 @@ def test_full_workload_in_the_bench_configuration():
     od, ld = parity.run_gpu(q, k, v, scale)
     assert bits_equal(oh, od)
     assert torch.equal(lh, ld)
+
+
+def test_concurrent_calls_from_two_threads():
+    """Two host threads, each with its own stream and workspace, call at the same
+    time (the library serialises its enqueue and reuses its events): every result
+    is still fa_fwd's bit for bit."""
+    import threading
+    cases = [inputs.make_random(1, 6, 900, 128, seed=95 + i) for i in range(2)]
+    results = [None, None]
+    errors = []
+
+    def worker(i):
+        try:
+            torch.cuda.set_device(0)
+            q, k, v = cases[i]
+            s = torch.cuda.Stream()
+            ws = torch.empty(fa.fa_fwd_host_workspace_bytes(1, 6, 900, 128), dtype=torch.uint8, device="cuda")
+            outs = []
+            for _ in range(5):
+                outs.append(fa.fa_fwd_host(q.pin_memory(), k.pin_memory(), v.pin_memory(), scale=0.08, num_chunks=3,
+                                           workspace=ws, stream=s))
+            s.synchronize()
+            results[i] = outs
+        except Exception as e:     # surfaced below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for i, (q, k, v) in enumerate(cases):
+        od, ld = parity.run_gpu(q, k, v, 0.08)
+        for oh, lh in results[i]:
+            assert bits_equal(oh, od)
+            assert torch.equal(lh, ld)
