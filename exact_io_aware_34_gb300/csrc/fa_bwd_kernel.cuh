@@ -31,6 +31,12 @@
 // The tile products of block i that read those results, then block i+1's dP
 // (into R[i&1]), follow in issue order, which the tensor core keeps.
 //
+// In the key-block kernel Q_i and dO_i share a ring slot but each has its own
+// full and empty barriers. dK (the last reader of Q_i) is issued before dV
+// (the last reader of dO_i), so the copy of Q into a freed slot starts one
+// tile product earlier than the copy of dO; S^T of the next block, which
+// needs Q alone, goes in as soon as its region is free and Q has landed.
+//
 // Warp roles (10 warps, as in the forward kernel):
 //   warps 0-7  elementwise step + epilogue: warp w serves TMEM lane quarter
 //              w & 3 (32 rows) and the 64 streamed-block columns
@@ -462,8 +468,10 @@ __global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
   constexpr uint32_t kColR = 2 * HD;    // R0 = kColR, R1 = kColR + 128
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_kv_full;
-  __shared__ __align__(8) uint64_t bar_in_full[C::kStages];
-  __shared__ __align__(8) uint64_t bar_in_empty[C::kStages];
+  __shared__ __align__(8) uint64_t bar_q_full[C::kStages];     // Q_i and -LSE*log2e landed
+  __shared__ __align__(8) uint64_t bar_q_empty[C::kStages];    // dK(i) done with Q_i
+  __shared__ __align__(8) uint64_t bar_do_full[C::kStages];    // dO_i and -D landed
+  __shared__ __align__(8) uint64_t bar_do_empty[C::kStages];   // dV(i) done with dO_i
   __shared__ __align__(8) uint64_t bar_s_full;
   __shared__ __align__(8) uint64_t bar_dp_free;
   __shared__ __align__(8) uint64_t bar_p_full;
@@ -489,8 +497,10 @@ __global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
   if (threadIdx.x == 0) {
     ptx::mbar_init(ptx::smem_u32(&bar_kv_full), 1);
     for (int s = 0; s < C::kStages; ++s) {
-      ptx::mbar_init(ptx::smem_u32(&bar_in_full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bar_in_empty[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bar_q_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bar_q_empty[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bar_do_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bar_do_empty[s]), 1);
     }
     ptx::mbar_init(ptx::smem_u32(&bar_s_full), 1);
     ptx::mbar_init(ptx::smem_u32(&bar_dp_free), 256);
@@ -527,35 +537,51 @@ __global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
         ptx::tma_load_3d(sK + c * C::kChunkBytes, &tmK, kv_full, c * 64, kv0, bh, pol_once);
         ptx::tma_load_3d(sV + c * C::kChunkBytes, &tmV, kv_full, c * 64, kv0, bh, pol_once);
       }
-      int issued = 0;
+      // Q_i (with its rows' -LSE*log2e) goes into its slot as soon as dK of
+      // the slot's previous block has completed, dO_i (with -D) once dV has:
+      // the issuer runs dK first, so S^T, which needs only Q, can start early.
+      int issued_q = 0, issued_do = 0;
       bool ok = true;
-      for (int i = 0; i < n; ++i) {
+      for (int i = 0; i < n && ok; ++i) {
         const int slot = i % C::kStages;
-        if (!wait_or_abort(ptx::smem_u32(&bar_in_empty[slot]), ((i / C::kStages) & 1) ^ 1u, abort_ptr,
-                           p.timeout_ns, kRoleDkvProducer)) {
+        const uint32_t par = ((i / C::kStages) & 1) ^ 1u;
+        const uint32_t dst = sRing + slot * C::kPairBytes;
+        const size_t voff = static_cast<size_t>(bh) * p.Npad + static_cast<size_t>(i) * C::kBlk;
+        if (!wait_or_abort(ptx::smem_u32(&bar_q_empty[slot]), par, abort_ptr, p.timeout_ns, kRoleDkvProducer)) {
           ok = false;
           break;
         }
-        issued = i + 1;
-        if (i == p.drop_load) continue;    // test hook: this step's tiles never arrive
-        const uint32_t full = ptx::smem_u32(&bar_in_full[slot]);
-        const uint32_t dst = sRing + slot * C::kPairBytes;
-        ptx::mbar_arrive_expect_tx(full, C::kPairBytes + C::kVecBytes);
-        for (int c = 0; c < C::kChunks; ++c) {
-          ptx::tma_load_3d(dst + c * C::kChunkBytes, &tmQ, full, c * 64, i * C::kBlk, bh, pol_shared);
-          ptx::tma_load_3d(dst + C::kTileBytes + c * C::kChunkBytes, &tmdO, full, c * 64, i * C::kBlk, bh,
-                           pol_shared);
+        issued_q = i + 1;
+        if (i != p.drop_load) {    // test hook: this step's tiles never arrive
+          const uint32_t full = ptx::smem_u32(&bar_q_full[slot]);
+          ptx::mbar_arrive_expect_tx(full, C::kTileBytes + C::kBlk * 4);
+          for (int c = 0; c < C::kChunks; ++c)
+            ptx::tma_load_3d(dst + c * C::kChunkBytes, &tmQ, full, c * 64, i * C::kBlk, bh, pol_shared);
+          ptx::bulk_load_1d(sVec + slot * C::kVecBytes, p.nlse2 + voff, C::kBlk * 4, full, pol_shared);
         }
-        const size_t voff = static_cast<size_t>(bh) * p.Npad + static_cast<size_t>(i) * C::kBlk;
-        ptx::bulk_load_1d(sVec + slot * C::kVecBytes, p.nlse2 + voff, C::kBlk * 4, full, pol_shared);
-        ptx::bulk_load_1d(sVec + slot * C::kVecBytes + C::kBlk * 4, p.ndelta + voff, C::kBlk * 4, full,
-                          pol_shared);
+        if (!wait_or_abort(ptx::smem_u32(&bar_do_empty[slot]), par, abort_ptr, p.timeout_ns, kRoleDkvProducer)) {
+          ok = false;
+          break;
+        }
+        issued_do = i + 1;
+        if (i != p.drop_load) {
+          const uint32_t full = ptx::smem_u32(&bar_do_full[slot]);
+          ptx::mbar_arrive_expect_tx(full, C::kTileBytes + C::kBlk * 4);
+          for (int c = 0; c < C::kChunks; ++c)
+            ptx::tma_load_3d(dst + C::kTileBytes + c * C::kChunkBytes, &tmdO, full, c * 64, i * C::kBlk, bh,
+                             pol_shared);
+          ptx::bulk_load_1d(sVec + slot * C::kVecBytes + C::kBlk * 4, p.ndelta + voff, C::kBlk * 4, full,
+                            pol_shared);
+        }
       }
       if (!ok || *abort_ptr) {
         drain_wait(kv_full, 0, p.timeout_ns);
-        for (int i = issued > C::kStages ? issued - C::kStages : 0; i < issued; ++i)
+        for (int i = issued_q > C::kStages ? issued_q - C::kStages : 0; i < issued_q; ++i)
           if (i != p.drop_load)
-            drain_wait(ptx::smem_u32(&bar_in_full[i % C::kStages]), (i / C::kStages) & 1, p.timeout_ns);
+            drain_wait(ptx::smem_u32(&bar_q_full[i % C::kStages]), (i / C::kStages) & 1, p.timeout_ns);
+        for (int i = issued_do > C::kStages ? issued_do - C::kStages : 0; i < issued_do; ++i)
+          if (i != p.drop_load)
+            drain_wait(ptx::smem_u32(&bar_do_full[i % C::kStages]), (i / C::kStages) & 1, p.timeout_ns);
       }
     }
     __syncwarp();
@@ -567,43 +593,59 @@ __global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
       auto region = [&](int i) { return tmem_base + kColR + 128u * static_cast<uint32_t>(i & 1); };
       auto q_tile = [&](int i) { return sRing + (i % C::kStages) * C::kPairBytes; };
       bool ok = wait_warp_or_abort(ptx::smem_u32(&bar_kv_full), 0, abort_ptr, p.timeout_ns, kRoleDkvMma);
-      if (ok) ok = wait_warp_or_abort(ptx::smem_u32(&bar_in_full[0]), 0, abort_ptr, p.timeout_ns, kRoleDkvMma);
+      if (ok) ok = wait_warp_or_abort(ptx::smem_u32(&bar_q_full[0]), 0, abort_ptr, p.timeout_ns, kRoleDkvMma);
       if (ok) {
         ptx::tc_fence_after();
         issue_tile_qk<HD>(region(0), sK, q_tile(0));                   // S_0^T = K Q_0^T
+      }
+      if (ok) ok = wait_warp_or_abort(ptx::smem_u32(&bar_do_full[0]), 0, abort_ptr, p.timeout_ns, kRoleDkvMma);
+      if (ok) {
+        ptx::tc_fence_after();
         issue_tile_qk<HD>(region(1), sV, q_tile(0) + C::kTileBytes);   // dP_0^T = V dO_0^T
         ptx::mma_commit_warp(ptx::smem_u32(&bar_s_full));
       }
       for (int i = 0; i < n && ok; ++i) {
-        // S_{i+1}^T goes in as soon as region(i+1) is free (dp_free(i)) if the
-        // (Q, dO) pair of block i+1 has already landed; a late pair must not
-        // hold back dV/dK(i), whose commit frees the ring slot the next copy
-        // needs.
+        // S_{i+1}^T goes in as soon as region(i+1) is free (dp_free(i)) and
+        // Q_{i+1} has landed, if that happens before p_full(i); otherwise
+        // after dK/dV(i). A late Q must not hold back dK/dV(i), whose commits
+        // free the ring slots the next copies need.
         bool s_issued = false;
         const int s1 = (i + 1) % C::kStages;
         const uint32_t in_par = ((i + 1) / C::kStages) & 1;
+        const uint32_t q_full1 = ptx::smem_u32(&bar_q_full[s1]);
         if (i + 1 < n) {
           ok = wait_warp_or_abort(ptx::smem_u32(&bar_dp_free), i & 1, abort_ptr, p.timeout_ns, kRoleDkvMma);
           if (!ok) break;
-          if (__all_sync(0xffffffffu, ptx::mbar_test_wait(ptx::smem_u32(&bar_in_full[s1]), in_par))) {
-            ptx::tc_fence_after();
-            issue_tile_qk<HD>(region(i + 1), sK, q_tile(i + 1));        // S_{i+1}^T
-            s_issued = true;
+          const uint64_t t0 = ptx::globaltimer_ns();
+          while (true) {
+            if (__all_sync(0xffffffffu, ptx::mbar_test_wait(q_full1, in_par))) {
+              ptx::tc_fence_after();
+              issue_tile_qk<HD>(region(i + 1), sK, q_tile(i + 1));      // S_{i+1}^T
+              s_issued = true;
+              break;
+            }
+            if (__all_sync(0xffffffffu, ptx::mbar_test_wait(ptx::smem_u32(&bar_p_full), i & 1))) break;
+            // Out of time or aborting: the bounded wait below reports it.
+            if (__any_sync(0xffffffffu, *abort_ptr != 0) || ptx::globaltimer_ns() - t0 > p.timeout_ns) break;
           }
         }
         ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_full), i & 1, abort_ptr, p.timeout_ns, kRoleDkvMma);
         if (!ok) break;
         ptx::tc_fence_after();
-        issue_tile_acc<HD, 64>(tmem_base + kColDV, region(i), q_tile(i) + C::kTileBytes, i > 0);   // dV += P^T dO_i
         issue_tile_acc<HD, 64>(tmem_base + kColDK, region(i) + 32, q_tile(i), i > 0);             // dK += dS^T Q_i
-        ptx::mma_commit_warp(ptx::smem_u32(&bar_in_empty[i % C::kStages]));
+        ptx::mma_commit_warp(ptx::smem_u32(&bar_q_empty[i % C::kStages]));
+        issue_tile_acc<HD, 64>(tmem_base + kColDV, region(i), q_tile(i) + C::kTileBytes, i > 0);   // dV += P^T dO_i
+        ptx::mma_commit_warp(ptx::smem_u32(&bar_do_empty[i % C::kStages]));
         if (i + 1 < n) {
           if (!s_issued) {
-            ok = wait_warp_or_abort(ptx::smem_u32(&bar_in_full[s1]), in_par, abort_ptr, p.timeout_ns, kRoleDkvMma);
+            ok = wait_warp_or_abort(q_full1, in_par, abort_ptr, p.timeout_ns, kRoleDkvMma);
             if (!ok) break;
             ptx::tc_fence_after();
             issue_tile_qk<HD>(region(i + 1), sK, q_tile(i + 1));        // S_{i+1}^T
           }
+          ok = wait_warp_or_abort(ptx::smem_u32(&bar_do_full[s1]), in_par, abort_ptr, p.timeout_ns, kRoleDkvMma);
+          if (!ok) break;
+          ptx::tc_fence_after();
           issue_tile_qk<HD>(region(i), sV, q_tile(i + 1) + C::kTileBytes);   // dP_{i+1}^T
           ptx::mma_commit_warp(ptx::smem_u32(&bar_s_full));
         }
