@@ -14,7 +14,7 @@ region; the max over ranks of the summed device time. For N > 1 (launched by
 torchrun) every rank runs its own copy of the workload (independent problems,
 no collective on the data path): weak scaling.
 
-The same run also times the backward pass (fa_bwd, three launches) on the
+The same run also times the backward pass (fa_bwd, two launches) on the
 same workload and reports it under "bwd" (skip with --no-bwd), and a decode
 shape with shared K/V heads (fa_fwd_kv: B=4, 32 query heads on 8 K/V heads,
 one query row against 32768 keys, d=128) under "decode" in K/V GB/s against
@@ -596,8 +596,8 @@ def run_native(args):
             "value": bwd_flops / (bwd_ms * 1e-3) / 1e12, "unit": UNIT, "steps": n_steps,
             "ms_per_step": bwd_ms,
             "step_ms": {"min": min(b_ms), "median": statistics.median(b_ms), "max": max(b_ms)},
-            "executed_tflops": 3.5 * flops / (bwd_ms * 1e-3) / 1e12,   # S and dP formed in both kernels
-            "gpu_launches": 3 * n_steps,
+            "executed_tflops": 3.5 * flops / (bwd_ms * 1e-3) / 1e12,   # S and dP formed in both CTA roles
+            "gpu_launches": 2 * n_steps,
             "workspace_bytes": ws_b.numel(),
             "clocks": bclocks.summary(),
         }
@@ -704,7 +704,7 @@ def run_native(args):
                                "unit": UNIT, "frac": bwd["value"] / peaks["bf16_tflops"],
                                "traffic": load_traffic(w.name, ":bwd", BWD_KERNEL_SOURCES),
                                "peak_source": f"{peak_src} dense bf16 burst",
-                               "kernels": "bwd_prep_kernel, fa_bwd_dq_kernel<%d>, fa_bwd_dkdv_kernel<%d>" % (d, d)}
+                               "kernels": "bwd_prep_kernel, fa_bwd_kernel<%d> (dK/dV and dQ CTAs)" % d}
             if cpu_bwd is not None:
                 bwd["cpu_baseline"] = cpu_bwd
             line["bwd"] = bwd

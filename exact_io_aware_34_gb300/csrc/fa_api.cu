@@ -268,12 +268,10 @@ fa_status_t bwd_launch(const void* Q, const void* K, const void* V, const void* 
   if (dev < 0 || dev >= 64) return FA_ERR_UNSUPPORTED;
   static std::once_flag once[64];
   static cudaError_t attr_err[64];
+  // Dynamic shared memory of the main kernel: the larger of its two roles.
+  constexpr int kSmem = fa::DqCfg<HD>::kSmemBytes > C::kSmemBytes ? fa::DqCfg<HD>::kSmemBytes : C::kSmemBytes;
   std::call_once(once[dev], [&] {
-    attr_err[dev] = cudaFuncSetAttribute(fa::fa_bwd_dq_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         fa::DqCfg<HD>::kSmemBytes);
-    if (attr_err[dev] == cudaSuccess)
-      attr_err[dev] = cudaFuncSetAttribute(fa::fa_bwd_dkdv_kernel<HD>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    attr_err[dev] = cudaFuncSetAttribute(fa::fa_bwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   });
   if (attr_err[dev] != cudaSuccess) return cuda_fail(attr_err[dev]);
 
@@ -295,6 +293,7 @@ fa_status_t bwd_launch(const void* Q, const void* K, const void* V, const void* 
   p.Npad = static_cast<int>(npad);
   p.H = H;
   p.n_blocks = static_cast<int>(npad / C::kBlk);
+  p.BH = BH;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
   p.scale = scale;
   p.timeout_ns = timeout_ns;
@@ -306,13 +305,10 @@ fa_status_t bwd_launch(const void* Q, const void* K, const void* V, const void* 
       static_cast<float*>(ws) + rows, N, p.Npad, rows);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
-  const dim3 grid(static_cast<unsigned>(p.n_blocks), H, B);
-  // 2. dQ, one CTA per 128 query rows
-  fa::fa_bwd_dq_kernel<HD><<<grid, C::kThreads, fa::DqCfg<HD>::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e);
-  // 3. dK and dV, one CTA per 128 key rows
-  fa::fa_bwd_dkdv_kernel<HD><<<grid, C::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
+  // 2. dK and dV (one CTA per 128 key rows), then dQ (one CTA per 128 query
+  // rows), in one launch
+  const unsigned ctas = static_cast<unsigned>(2LL * p.n_blocks * BH);
+  fa::fa_bwd_kernel<HD><<<ctas, C::kThreads, kSmem, stream>>>(mq, mk, mv, mdo, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   return FA_OK;

@@ -8,17 +8,19 @@
 //   dP = dO V^T                         dS = P * (dP - D),  D_i = dO_i . O_i
 //   dQ = scale dS K                     dK = scale dS^T Q
 //
-// Three launches on the caller's stream:
+// Two launches on the caller's stream:
 //   bwd_prep_kernel     per query row: -D and -LSE*log2(e) into a workspace
 //                       whose rows are padded to a multiple of 128; padding
 //                       rows get 0 and -inf, so their probabilities are zero.
-//   fa_bwd_dq_kernel    one CTA per 128 query rows of one (b, h), streaming
-//                       the K/V blocks: S = Q K_j^T, dP = dO V_j^T, dS,
-//                       dQ += dS K_j.
-//   fa_bwd_dkdv_kernel  one CTA per 128 key rows of one (b, h), streaming the
-//                       Q/dO blocks: S^T = K Q_i^T, dP^T = V dO_i^T, P^T,
-//                       dS^T, dV += P^T dO_i, dK += dS^T Q_i.
-// S and dP are formed in both kernels (7 tile products per pair of blocks
+//   fa_bwd_kernel       CTAs of two roles:
+//     key block (bwd_dkdv_cta)   one CTA per 128 key rows of one (b, h),
+//                       streaming the Q/dO blocks: S^T = K Q_i^T,
+//                       dP^T = V dO_i^T, P^T, dS^T, dV += P^T dO_i,
+//                       dK += dS^T Q_i;
+//     query block (bwd_dq_cta)   one CTA per 128 query rows of one (b, h),
+//                       streaming the K/V blocks: S = Q K_j^T, dP = dO V_j^T,
+//                       dS, dQ += dS K_j.
+// S and dP are formed in both roles (7 tile products per pair of blocks
 // instead of 5). In exchange every accumulator stays in the TMEM of the one
 // CTA that owns it: no atomics, a deterministic result, and the state fits
 // TMEM (512 columns): the key-block owner holds dV and dK (2 x d columns)
@@ -86,6 +88,7 @@ struct BwdParams {
   int Npad;               // N rounded up to a multiple of 128
   int H;
   int n_blocks;           // Npad / 128
+  int BH;                 // B * H
   float scale_log2;       // scale * log2(e)
   float scale;
   unsigned long long timeout_ns;
@@ -205,11 +208,11 @@ struct DqCfg {
   static constexpr uint32_t kColDS = HD + 256;    // + 64 * (j & 1)
 };
 
+// One CTA of the query-block role: query rows [128 blk, 128 blk + 128) of
+// head bh. The tensor maps are the kernel's own (grid-constant) parameters.
 template <int HD>
-__global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
-    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                     const BwdParams p) {
+__device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                           const CUtensorMap& tmdO, const BwdParams& p, int blk, int bh) {
   using C = BwdCfg<HD>;
   using D = DqCfg<HD>;
   extern __shared__ uint8_t smem_raw[];
@@ -228,8 +231,7 @@ __global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.z * p.H + blockIdx.y;
-  const int q0 = blockIdx.x * C::kBlk;
+  const int q0 = blk * C::kBlk;
   const int n = p.n_blocks;
 
   const uint32_t smem_base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -457,11 +459,10 @@ __global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
 }
 
 // ---------------------------------------------------------------- dK, dV
+// One CTA of the key-block role: key rows [128 blk, 128 blk + 128) of head bh.
 template <int HD>
-__global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
-    fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                       const BwdParams p) {
+__device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                             const CUtensorMap& tmdO, const BwdParams& p, int blk, int bh) {
   using C = BwdCfg<HD>;
   constexpr uint32_t kColDV = 0;
   constexpr uint32_t kColDK = HD;
@@ -482,8 +483,7 @@ __global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.z * p.H + blockIdx.y;
-  const int kv0 = blockIdx.x * C::kBlk;
+  const int kv0 = blk * C::kBlk;
   const int n = p.n_blocks;
 
   const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -740,6 +740,28 @@ __global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, C::kTmemCols);
   }
+}
+
+// Both roles in one launch, on a 1-D grid: the n_blocks * B * H key-block
+// CTAs first, then as many query-block CTAs. Blocks are dispatched in index
+// order and a key-block CTA does four tile products per step against three,
+// so the longer CTAs start first and the shorter ones fill the last wave of
+// SMs, where two launches would each leave a part of their last wave idle.
+template <int HD>
+__global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
+    fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                  const BwdParams p) {
+  const long long per_role = static_cast<long long>(p.n_blocks) * p.BH;
+  long long idx = blockIdx.x;
+  const bool dkdv = idx < per_role;
+  if (!dkdv) idx -= per_role;
+  const int blk = static_cast<int>(idx % p.n_blocks);
+  const int bh = static_cast<int>(idx / p.n_blocks);
+  if (dkdv)
+    bwd_dkdv_cta<HD>(tmQ, tmK, tmV, tmdO, p, blk, bh);
+  else
+    bwd_dq_cta<HD>(tmQ, tmK, tmV, tmdO, p, blk, bh);
 }
 
 }  // namespace fa

@@ -111,8 +111,8 @@ fa_status_t fa_fwd_host(const void* Qh, const void* Kh, const void* Vh, void* Oh
  * FA_ERR_TIMEOUT if any kernel of this library on this device gave up on a
  * wait since the last call, or FA_ERR_CUDA if the synchronisation failed.
  * `info`, if not NULL, receives 4 words describing the first timeout:
- * {role (forward: 1 producer, 2 mma, 3 softmax/epilogue; backward dQ kernel:
- * 4, 5, 6; backward dK/dV kernel: 7, 8, 9; short-query kernel of fa_fwd_kv:
+ * {role (forward: 1 producer, 2 mma, 3 softmax/epilogue; backward dQ CTA:
+ * 4, 5, 6; backward dK/dV CTA: 7, 8, 9; short-query kernel of fa_fwd_kv:
  * 10, 11, 12, in the same order), blockIdx.x, blockIdx.y,
  * blockIdx.z}; all zero when there was none.
  */
@@ -275,9 +275,9 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N);
  *   workspace      : device, at least fa_bwd_workspace_bytes(B, H, N) bytes,
  *                    128-byte aligned, owned by the caller; overwritten.
  *   B, H, N, d, scale, stream : as for fa_fwd (same limits).
- * Three kernel launches on `stream`: a per-row pass over O and dO, then the
- * dQ kernel (one CTA per 128 query rows) and the dK/dV kernel (one CTA per
- * 128 key rows). Inputs must be 16-byte aligned (LSE 4-byte); dQ, dK, dV and
+ * Two kernel launches on `stream`: a per-row pass over O and dO, then one
+ * launch whose CTAs take one of two roles: dK/dV (one CTA per 128 key rows)
+ * or dQ (one CTA per 128 query rows). Inputs must be 16-byte aligned (LSE 4-byte); dQ, dK, dV and
  * the workspace must not overlap any input or each other. Errors as for
  * fa_fwd, plus FA_ERR_INVALID_ARG for a missing, misaligned, too small or
  * overlapping output or workspace.
@@ -305,9 +305,9 @@ fa_status_t fa_fwd_fault_test(const void* Q, const void* K, const void* V, void*
 /*
  * fa_bwd_fault_test -- TEST HOOK, not for production use. Same as fa_bwd, but
  * every device-side wait gives up after `timeout_ns` nanoseconds, and when
- * `drop_load` >= 0 each backward kernel's producer skips one tile load in
- * every CTA: in the dQ kernel the drop_load-th of K_0, V_0, K_1, V_1, ...; in
- * the dK/dV kernel the (Q, dO) pair of query block drop_load. The waiting
+ * `drop_load` >= 0 the producer of every CTA skips one tile load: in a dQ
+ * CTA the drop_load-th of K_0, V_0, K_1, V_1, ...; in a dK/dV CTA the Q and
+ * dO tiles of query block drop_load. The waiting
  * role then gives up, every role stops, waits for its own copies and
  * tensor-core work in flight, frees its tensor memory and exits;
  * fa_get_device_status reports FA_ERR_TIMEOUT and the CUDA context stays

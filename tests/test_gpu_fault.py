@@ -53,9 +53,9 @@ def test_drop_beyond_last_load_is_harmless():
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("drop", [0, 1, 3, 6])
 def test_backward_dropped_load_times_out_cleanly(d, drop):
-    """The same for fa_bwd: one K/V load of the dQ kernel and one Q/dO load of
-    the dK/dV kernel never arrive; both kernels end with a timeout status, and
-    the next backward call in the same context is correct."""
+    """The same for fa_bwd: one K/V load of every dQ CTA and the Q/dO loads of
+    one block in every dK/dV CTA never arrive; the launch ends with a timeout
+    status, and the next backward call in the same context is correct."""
     B, H, N = 1, 2, 700
     s = 1 / math.sqrt(d)
     q, k, v = inputs.make_random(B, H, N, d, seed=40 + drop)
