@@ -350,34 +350,44 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
       ok = wait_warp_or_abort(ptx::smem_u32(&bar_s_full[t]), j & 1, abort_ptr, p.timeout_ns, kRoleSoftmax);
       if (!ok) break;
       ptx::tc_fence_after();
+      // The loads also reduce each 32-column piece to its maximum, which is
+      // the row maximum of a full block. In the ragged last block the
+      // columns past N hold scores of zero-filled keys, so that block masks
+      // them to -inf and takes the maximum itself.
       uint32_t s[4][32];
+      float mr[4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + 32 * c, s[c]);
+      for (int c = 0; c < 4; ++c) ptx::tmem_ld32_max(tS + 32 * c, s[c], mr[c]);
       ptx::tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) ptx::reg_fence32(s[c]);
+      for (int c = 0; c < 4; ++c) {
+        ptx::reg_fence32(s[c]);
+        ptx::reg_fence1(mr[c]);
+      }
 
       const int valid = p.N_kv - j * C::kBN;    // keys of this block that exist
       const bool ragged = valid < C::kBN;
-      if (ragged) {
+      float mt;
+      if (!ragged) {
+        mt = ptx::max3(mr[0], mr[1], fmaxf(mr[2], mr[3]));
+      } else {
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int i = 0; i < 32; ++i)
             if (32 * c + i >= valid) s[c][i] = __float_as_uint(-INFINITY);
-      }
-      // Row maximum: 8 independent chains of 3-input max, then a small tree.
-      float mc[8];
+        // Row maximum: 8 independent chains of 3-input max, then a small tree.
+        float mc[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int c = k >> 1, b = (k & 1) * 16;
-        mc[k] = fmaxf(__uint_as_float(s[c][b]), __uint_as_float(s[c][b + 1]));
+        for (int k = 0; k < 8; ++k) {
+          const int c = k >> 1, b = (k & 1) * 16;
+          mc[k] = fmaxf(__uint_as_float(s[c][b]), __uint_as_float(s[c][b + 1]));
 #pragma unroll
-        for (int i = 2; i < 16; i += 2)
-          mc[k] = ptx::max3(mc[k], __uint_as_float(s[c][b + i]), __uint_as_float(s[c][b + i + 1]));
+          for (int i = 2; i < 16; i += 2)
+            mc[k] = ptx::max3(mc[k], __uint_as_float(s[c][b + i]), __uint_as_float(s[c][b + i + 1]));
+        }
+        mt = ptx::max3(ptx::max3(mc[0], mc[1], mc[2]), ptx::max3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
       }
-      const float mt = ptx::max3(ptx::max3(mc[0], mc[1], mc[2]), ptx::max3(mc[3], mc[4], mc[5]),
-                                 fmaxf(mc[6], mc[7]));
 
       float alpha = 1.f;
       bool rescale_o = false;

@@ -346,6 +346,20 @@ __device__ __forceinline__ void reg_fence32(uint32_t (&r)[32]) {
   asm volatile("" : FA_M8(r, 0), FA_M8(r, 8), FA_M8(r, 16), FA_M8(r, 24));
 }
 
+// tmem_ld32 that also returns, in `mx`, the maximum of the 32 fp32 values
+// this thread loads (the load-with-reduction form of sm_103a; NaN operands
+// are ignored, as by max.f32). Valid after tmem_ld_wait, like the values.
+__device__ __forceinline__ void tmem_ld32_max(uint32_t taddr, uint32_t (&r)[32], float& mx) {
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, %32, [%33];"
+      : FA_R8(r, 0), FA_R8(r, 8), FA_R8(r, 16), FA_R8(r, 24), "=f"(mx)
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void reg_fence1(float& x) { asm volatile("" : "+f"(x)); }
+
 #undef FA_R8
 #undef FA_W8
 #undef FA_M8
