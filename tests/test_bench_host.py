@@ -100,3 +100,29 @@ def test_cpu_baseline_single_core():
     r = bench.cpu_baseline_single_core("n256_d64", target_s=0.2)
     assert r["kind"] == "oracle" and r["cores"] == 1 and r["unit"] == "TFLOP/s" and r["value"] > 0
     assert r["workload"] == "n256_d64"
+
+
+def test_committed_traffic_records_match_their_profiles():
+    """Each record of profiles/dram_traffic.json adds up, and the ncu summary it
+    comes from names the same kernel-sources hash. Where the record is current
+    for the forward, its DRAM bytes are within a factor 1.5 of the algorithmic
+    O(N d) bytes (inputs once, outputs once), far below the N^2 traffic of
+    materialised scores."""
+    with open(bench.TRAFFIC_FILE) as f:
+        rec = json.load(f)
+    summaries = {
+        "prefill8k_d128_h32": "fa_fwd_kernel_prefill8k_d128.md",
+        "prefill8k_d128_h32:bwd": "fa_bwd_kernels_prefill8k_d128.md",
+        "decode32k_gqa8_b4": "fa_decode_kernel_decode32k_gqa8.md",
+    }
+    assert set(rec) == set(summaries)
+    for key, md in summaries.items():
+        e = rec[key]
+        assert e["dram_bytes_read"] + e["dram_bytes_write"] == e["dram_bytes_per_launch"], key
+        with open(os.path.join(os.path.dirname(bench.TRAFFIC_FILE), md)) as f:
+            assert e["kernel_source_hash"] in f.read(), (key, md)
+    traffic = bench.load_traffic("prefill8k_d128_h32")
+    if traffic is not None:
+        B, H, N, d = 1, 32, 8192, 128
+        algorithmic = B * H * N * (8 * d + 4)
+        assert algorithmic / 1.5 <= traffic <= 1.5 * algorithmic
