@@ -555,6 +555,9 @@ fa_status_t bwd_impl(const void* Q, const void* K, const void* V, const void* O,
                      size_t workspace_bytes, int drop_load, unsigned long long timeout_ns, cudaStream_t stream) {
   fa_status_t st = check_args(Q, K, V, O, LSE, B, H, N, d, scale);
   if (st != FA_OK) return st;
+  // The main launch is a 1-D grid: one CTA per 128 rows of every head, in
+  // each of its two roles.
+  if (2LL * (bwd_npad(N) / 128) * B * H > 2147483647LL) return FA_ERR_UNSUPPORTED;
   if (!dO || !dQ || !dK || !dV || !workspace) return FA_ERR_INVALID_ARG;
   for (const void* ptr : {dO, static_cast<const void*>(dQ), static_cast<const void*>(dK),
                           static_cast<const void*>(dV)})

@@ -280,7 +280,8 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N);
  * or dQ (one CTA per 128 query rows). Inputs must be 16-byte aligned (LSE 4-byte); dQ, dK, dV and
  * the workspace must not overlap any input or each other. Errors as for
  * fa_fwd, plus FA_ERR_INVALID_ARG for a missing, misaligned, too small or
- * overlapping output or workspace.
+ * overlapping output or workspace, and FA_ERR_UNSUPPORTED when
+ * 2 * ceil(N / 128) * B * H exceeds 2^31 - 1 (the CTA count of the main launch).
  */
 fa_status_t fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
                    const float* LSE, void* dQ, void* dK, void* dV,

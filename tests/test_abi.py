@@ -165,6 +165,10 @@ def test_bwd_workspace_size(lib):
     (dict(scale=-1.0), fa.FA_ERR_UNSUPPORTED),
     (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
     (dict(N=0), fa.FA_ERR_INVALID_ARG),
+    # 2 * B * H CTAs, past the 1-D grid limit (inputs spaced 1 TiB apart, so
+    # that only the size is wrong)
+    (dict(B=65535, H=32768, N=1, **{n: (1 << 44) + (i << 40) for i, n in enumerate(("Q", "K", "V", "O", "L"))}),
+     fa.FA_ERR_UNSUPPORTED),
 ])
 def test_bwd_host_side_rejections(lib, kwargs, expect):
     assert bwd_call(lib, **kwargs) == expect
