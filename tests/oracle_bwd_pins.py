@@ -95,3 +95,36 @@ def pin_bwd_library_autograd(bwd):
 
 ALL_BWD_PINS = [pin_bwd_finite_difference, pin_bwd_n1, pin_bwd_equal_keys, pin_bwd_column_sums,
                 pin_bwd_library_autograd]
+
+
+# --- the bf16 materialise-path backward (the "twice the baseline" reference) ----
+def _torch_bf16_autograd(q, k, v, do, s):
+    """torch's own bf16 CPU autograd of standard attention: S = q k^T (bf16),
+    S * scale (bf16), a bf16 softmax (float32 inside, bf16 out), O = P v (bf16),
+    then O.backward(dO). Returns (dQ, dK, dV) as float64 numpy."""
+    import torch
+    tq, tk, tv = (x.clone().requires_grad_(True) for x in (q, k, v))
+    O = torch.softmax((tq @ tk.transpose(-1, -2)) * s, dim=-1) @ tv
+    O.backward(do)
+    return tuple(t.grad.float().numpy().astype(np.float64) for t in (tq, tk, tv))
+
+
+def pin_naive_bwd_torch_bf16_autograd(naive_bwd):
+    """``naive_bwd(Q, K, V, dO, scale)`` against torch's bf16 autograd of the
+    materialise path, element by element. Both store the same intermediates in
+    bf16 and sum in float32, so almost every element is identical; a float32
+    summation order that differs flips a bf16 rounding now and then (one ulp of
+    P, dS or a gradient element, seen large only where dQ cancels to near zero).
+    So: at least 98% identical elements, and every element within 2^-6 of its
+    own size plus 2^-9 of the gradient's largest element."""
+    import torch
+    g = torch.Generator().manual_seed(46)
+    for (B, H, N, d, s) in [(1, 2, 96, 64, 0.125), (1, 1, 200, 32, 0.3), (2, 1, 130, 16, 1.7)]:
+        q, k, v, do = (torch.randn(B, H, N, d, generator=g).to(torch.bfloat16) for _ in range(4))
+        want = _torch_bf16_autograd(q, k, v, do, s)
+        got = naive_bwd(*(x.float().numpy().astype(np.float64) for x in (q, k, v, do)), s)
+        for name, T, M in zip(("dQ", "dK", "dV"), want, got):
+            same = float(np.mean(T == M))
+            assert same >= 0.98, (name, N, d, s, same)
+            bound = 2.0 ** -6 * np.abs(T) + 2.0 ** -9 * np.abs(T).max()
+            assert np.all(np.abs(T - M) <= bound), (name, N, d, s, float(np.abs(T - M).max()))

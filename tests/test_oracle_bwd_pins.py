@@ -75,6 +75,58 @@ def test_naive_bf16_bwd_error_is_bf16_sized():
         assert 1e-6 < err < 3e-2 * np.abs(X).max(), err
 
 
+def test_naive_bf16_bwd_matches_torch_bf16_autograd():
+    """The reference agrees with torch's bf16 CPU autograd of the materialise
+    path element by element (rare one-ulp flips from float32 summation order)."""
+    pins.pin_naive_bwd_torch_bf16_autograd(oracle.naive_bf16_attention_bwd)
+
+
+def _naive_bwd_variant(change):
+    """The bf16 materialise-path backward written out again with one planted
+    change, for checking that the torch-autograd pin sees it."""
+    def bwd(Q, K, V, dO, scale):
+        s32 = np.float32(scale)
+        rnd = oracle.bf16_round
+
+        def one(q, k, v, do):
+            S = rnd(rnd(q @ k.T) * s32)
+            m = S.max(axis=1, keepdims=True)
+            e = np.exp(S - m, dtype=np.float32)
+            P32 = e / e.sum(axis=1, keepdims=True, dtype=np.float32)
+            P = rnd(P32)
+            dv = rnd(P.T @ do)
+            dP = do @ v.T if change == "dp_not_rounded" else rnd(do @ v.T)
+            Pb = P32 if change == "p_unrounded_in_softmax_grad" else P
+            if change == "d_from_o":
+                D = np.sum(do * rnd(P @ v), axis=1, keepdims=True, dtype=np.float32)
+            else:
+                D = np.sum(Pb * dP, axis=1, keepdims=True, dtype=np.float32)
+            dS = rnd(Pb * (dP - D))
+            if change != "scale_missing_from_ds":
+                dS = rnd(dS * s32)
+            return rnd(dS @ k), rnd(dS.T @ q), dv
+
+        Qf, Kf, Vf, dOf = (np.asarray(x, dtype=np.float32) for x in (Q, K, V, dO))
+        out = [np.empty(Qf.shape) for _ in range(3)]
+        for b in range(Qf.shape[0]):
+            for h in range(Qf.shape[1]):
+                for X, g in zip(out, one(Qf[b, h], Kf[b, h], Vf[b, h], dOf[b, h])):
+                    X[b, h] = g
+        return out
+    return bwd
+
+
+def test_naive_bwd_variant_without_change_passes():
+    pins.pin_naive_bwd_torch_bf16_autograd(_naive_bwd_variant(None))
+
+
+@pytest.mark.parametrize("change", ["scale_missing_from_ds", "dp_not_rounded", "d_from_o",
+                                    "p_unrounded_in_softmax_grad"])
+def test_planted_naive_bwd_mistake_is_caught(change):
+    with pytest.raises(AssertionError):
+        pins.pin_naive_bwd_torch_bf16_autograd(_naive_bwd_variant(change))
+
+
 def test_naive_bf16_bwd_heads_matches_full():
     r = np.random.default_rng(45)
     Q, K, V, dO = (oracle.bf16_round(r.standard_normal((2, 2, 40, 8))).astype(np.float64) for _ in range(4))
