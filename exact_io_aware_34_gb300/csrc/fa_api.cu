@@ -237,15 +237,31 @@ fa_status_t check_args(const void* Q, const void* K, const void* V, const void* 
   return FA_OK;
 }
 
-// Device address of g_naive_static_scratch on the current device, looked up
-// once per device (the first fa_naive_fwd_noalloc call on that device).
+// Device address of g_naive_static_scratch on the current device. The first
+// successful lookup on a device is kept; a failed one is not (its error is
+// returned and cleared from the runtime's last-error state), so the next call
+// on that device looks the address up again.
 cudaError_t naive_static_scratch(int dev, void** out) {
-  static std::once_flag once[64];
+  static std::mutex mu;
   static void* addr[64];
-  static cudaError_t err[64];
-  std::call_once(once[dev], [&] { err[dev] = cudaGetSymbolAddress(&addr[dev], g_naive_static_scratch); });
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_naive_static_scratch);
+    if (e != cudaSuccess || !p) {
+      (void)cudaGetLastError();
+      return e != cudaSuccess ? e : cudaErrorInvalidSymbol;
+    }
+    addr[dev] = p;
+  }
   *out = addr[dev];
-  return err[dev];
+  return cudaSuccess;
+}
+
+// The standard-attention launches put B*H in gridDim.z and the 128-row block
+// count of N in gridDim.y, both limited to 65535.
+bool naive_grid_ok(int B, int H, int N) {
+  return static_cast<long long>(B) * H <= 65535 && (static_cast<long long>(N) + 127) / 128 <= 65535;
 }
 
 // A correct pipeline never waits anywhere near this long; it only bounds
@@ -513,6 +529,7 @@ fa_status_t fa_naive_fwd(const void* Q, const void* K, const void* V, void* O, f
                          int d, float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   fa_status_t st = check_args(Q, K, V, O, LSE, B, H, N, d, scale);
   if (st != FA_OK) return st;
+  if (!naive_grid_ok(B, H, N)) return FA_ERR_UNSUPPORTED;
   if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 128 != 0) return FA_ERR_INVALID_ARG;
   const size_t need = fa_naive_workspace_bytes(B, H, N);
   if (workspace_bytes < need) return FA_ERR_INVALID_ARG;
@@ -530,6 +547,7 @@ fa_status_t fa_naive_fwd_noalloc(const void* Q, const void* K, const void* V, vo
   fa_status_t st = check_args(Q, K, V, O, LSE, B, H, N, d, scale);
   if (st != FA_OK) return st;
   if (fa_naive_workspace_bytes(B, H, N) > kNaiveStaticScratchBytes) return FA_ERR_UNSUPPORTED;
+  if (!naive_grid_ok(B, H, N)) return FA_ERR_UNSUPPORTED;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);

@@ -143,7 +143,9 @@ size_t fa_naive_workspace_bytes(int B, int H, int N);
  * fa_naive_workspace_bytes(B, H, N) bytes, 128-byte aligned, owned by the
  * caller, not overlapping any other buffer; its contents are overwritten.
  * Same shape limits and error codes as fa_fwd; FA_ERR_INVALID_ARG also for
- * a missing, misaligned, too small or overlapping workspace.
+ * a missing, misaligned, too small or overlapping workspace, and
+ * FA_ERR_UNSUPPORTED (before any CUDA call) when B*H > 65535 or
+ * ceil(N / 128) > 65535 (the launches' grid limits).
  */
 fa_status_t fa_naive_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
                          int B, int H, int N, int d, float scale,
@@ -162,9 +164,11 @@ fa_status_t fa_naive_fwd(const void* Q, const void* K, const void* V, void* O, f
  * 64 MiB return FA_ERR_UNSUPPORTED without launching anything (for example
  * B*H = 8 heads of N = 2048, or one head of N = 5760, still fit).
  *   - The call allocates nothing (no cudaMalloc, no library allocator).
+ *   - The B*H and N limits of fa_naive_fwd apply too (FA_ERR_UNSUPPORTED).
  *   - The first call on a device looks the array's device address up
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture. A failed lookup returns FA_ERR_CUDA and is
+ *     not remembered: the next call on that device tries again.
  *   - Every call on a device shares the one array, and the array keeps the
  *     last call's contents (nothing in it needs to start at zero). Calls whose
  *     kernels overlap on the GPU (different streams, no ordering between them)

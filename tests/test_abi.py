@@ -126,6 +126,20 @@ def test_naive_host_side_rejections(lib, kwargs, expect):
     assert naive_call(lib, **kwargs) == expect
 
 
+# B*H = 65536 heads of one row: past the launches' gridDim.z limit, and inside
+# the no-allocation array (65536 rows of 64 bf16 scores = 8 MiB); inputs spaced
+# 1 TiB apart so that only the head count is wrong. Rejected before any CUDA call.
+BIG_BH = dict(B=2, H=32768, N=1, **{n: (1 << 44) + (i << 40) for i, n in enumerate(("Q", "K", "V", "O", "L"))})
+
+
+def test_naive_rejects_head_counts_past_the_grid_limit(lib):
+    assert naive_call(lib, ws=(1 << 44) + (6 << 40), **BIG_BH) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_naive_workspace_bytes(2, 32768, 1) <= 64 << 20
+    st = lib.fa_naive_fwd_noalloc(BIG_BH["Q"], BIG_BH["K"], BIG_BH["V"], BIG_BH["O"], BIG_BH["L"], 2, 32768, 1, 128,
+                                  ctypes.c_float(0.1), None)
+    assert st == fa.FA_ERR_UNSUPPORTED
+
+
 def bwd_call(lib, **kw):
     args = dict(Q=A, K=A + GAP, V=A + 2 * GAP, O=A + 3 * GAP, L=A + 4 * GAP, dO=A + 5 * GAP, dQ=A + 6 * GAP,
                 dK=A + 7 * GAP, dV=A + 8 * GAP, ws=A + 9 * GAP, ws_bytes=1 << 40, B=1, H=1, N=128, d=128,

@@ -16,7 +16,6 @@ import pytest
 import torch
 
 from exact_io_aware_34_gb300 import fa, inputs
-from tests import parity
 
 pytestmark = pytest.mark.gpu
 
@@ -47,9 +46,10 @@ def test_noalloc_matches_workspace_entry_twice(d):
         torch.cuda.synchronize()
         assert torch.cuda.memory_allocated() <= before      # nothing was allocated through torch
         assert fa.fa_get_device_status()[0] == fa.FA_OK
-        dO = (o.float() - o_ref.float()).abs().max().item()
-        dL = (lse - lse_ref).abs().max().item()
-        assert dO <= parity.TOL_O_MAX and dL <= parity.TOL_LSE_MAX, (dO, dL)
+        # The same three deterministic kernels on the same inputs, with only
+        # the scratch memory moved: the results are equal bit for bit.
+        assert torch.equal(o.view(torch.int16), o_ref.view(torch.int16))
+        assert torch.equal(lse.view(torch.int32), lse_ref.view(torch.int32))
 
 
 def test_noalloc_makes_no_device_allocation():
