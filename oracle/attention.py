@@ -68,12 +68,14 @@ def bf16_round(x) -> np.ndarray:
 
     bfloat16 is the upper 16 bits of an IEEE float32. Rounding to nearest-even
     adds 0x7FFF plus the lowest kept bit, then truncates the low 16 bits.
-    NaN is passed through unchanged.
+    The sum stays below 2^32 for every non-NaN bit pattern (the largest,
+    -inf = 0xFF800000, reaches 0xFF807FFF), so 32-bit unsigned arithmetic is
+    exact. NaN is passed through unchanged.
     """
     x = np.ascontiguousarray(x, dtype=np.float32)
-    u = x.view(np.uint32).astype(np.uint64)
-    keep_lsb = (u >> np.uint64(16)) & np.uint64(1)
-    r = ((u + np.uint64(0x7FFF) + keep_lsb) & np.uint64(0xFFFF0000)).astype(np.uint32)
+    u = x.view(np.uint32)
+    keep_lsb = (u >> np.uint32(16)) & np.uint32(1)
+    r = (u + (np.uint32(0x7FFF) + keep_lsb)) & np.uint32(0xFFFF0000)
     out = r.view(np.float32)
     return np.where(np.isnan(x), x, out)
 

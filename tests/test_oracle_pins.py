@@ -140,6 +140,13 @@ def test_bf16_round_matches_torch():
         (np.arange(1, 2000, dtype=np.uint32) << 16 | 0x8000).view(np.float32),
         np.array([0.0, -0.0, np.inf, -np.inf, 3.3895314e38, 1e-45, -1e-45], dtype=np.float32),
     ])
+    # a stride through every 32-bit pattern, and the largest finite values and
+    # infinities of both signs (where a 32-bit sum would come closest to wrapping)
+    sweep = np.arange(0, 1 << 32, 65537, dtype=np.uint64).astype(np.uint32)
+    edges = np.array([0x7F7FFFFF, 0xFF7FFFFF, 0x7F7F8000, 0xFF7F8000, 0x7F800000, 0xFF800000, 0x7F7F7FFF,
+                      0xFF7F7FFF], dtype=np.uint32)
+    bits = np.concatenate([sweep, edges]).view(np.float32)
+    x = np.concatenate([x, bits[~np.isnan(bits)]])
     mine = oracle.bf16_round(x)
     ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy()
     np.testing.assert_array_equal(mine.view(np.uint32), ref.view(np.uint32))
