@@ -171,3 +171,80 @@ def check_bwd_full(q, k, v, do, scale, two_x_rule=True):
     err = bwd_errors(got, ref, naive)
     assert_bwd_within(err, two_x_rule)
     return err, got
+
+
+# --- whole-output parity at full size -------------------------------------------
+# Every output row of a full-size workload against the oracle, evaluated by a
+# pool of spawned single-threaded processes (one per host core): the inputs and
+# the GPU's O and LSE go to .npy files that every worker maps read-only, and
+# each task returns error statistics for one block of query rows of one head.
+def _full_rows_task(args):
+    folder, b, h, r0, r1, scale, two_x_rule = args
+    import os as _os
+    load = lambda n: np.load(_os.path.join(folder, n + ".npy"), mmap_mode="r")  # noqa: E731
+    q, k, v, o, lse = (load(n) for n in ("q", "k", "v", "o", "lse"))
+    Q = np.asarray(q[b:b + 1, h:h + 1, r0:r1], dtype=np.float64)
+    K = np.asarray(k[b:b + 1, h:h + 1], dtype=np.float64)
+    V = np.asarray(v[b:b + 1, h:h + 1], dtype=np.float64)
+    O_ref, L_ref = oracle.attention(Q, K, V, scale)
+    og = np.asarray(o[b:b + 1, h:h + 1, r0:r1], dtype=np.float64)
+    lg = np.asarray(lse[b:b + 1, h:h + 1, r0:r1], dtype=np.float64)
+    e = og - O_ref
+    out = {
+        "rows": r1 - r0,
+        "o_max": float(np.abs(e).max()),
+        "err_sq": float(np.sum(e * e)),
+        "ref_sq": float(np.sum(O_ref * O_ref)),
+        "lse_max": float(np.abs(lg - L_ref).max()),
+        "finite": bool(np.isfinite(og).all() and np.isfinite(lg).all()),
+    }
+    if two_x_rule:
+        On = oracle.naive_bf16_attention(Q, K, V, scale)
+        out["naive_o_max"] = float(np.abs(On - O_ref).max())
+    return out
+
+
+def check_full_parallel(q, k, v, scale, folder, two_x_rule=True, row_block=1024, workers=None):
+    """Full-size run on the GPU, then every output row compared with the
+    oracle (and the bf16 materialise-path reference for the 2x rule) by a
+    spawned process pool. Asserts the same tolerances as :func:`check_full`
+    over all B*H*N rows and returns the aggregated figures."""
+    import multiprocessing as mp
+    import os
+    B, H, N, d = q.shape
+    o, lse = run_gpu(q, k, v, scale)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("lse", lse)):
+        np.save(os.path.join(folder, name + ".npy"), t.float().numpy())
+    tasks = [(str(folder), b, h, r0, min(N, r0 + row_block), float(scale), two_x_rule)
+             for b in range(B) for h in range(H) for r0 in range(0, N, row_block)]
+    n = workers or len(os.sched_getaffinity(0))
+    saved = {x: os.environ.get(x) for x in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")}
+    for x in saved:
+        os.environ[x] = "1"
+    try:
+        with mp.get_context("spawn").Pool(n) as pool:
+            parts = pool.map(_full_rows_task, tasks, chunksize=1)
+    finally:
+        for x, val in saved.items():
+            if val is None:
+                os.environ.pop(x, None)
+            else:
+                os.environ[x] = val
+    err = {
+        "rows_checked": sum(p["rows"] for p in parts),
+        "rows_total": B * H * N,
+        "o_max": max(p["o_max"] for p in parts),
+        "o_fro": float(np.sqrt(sum(p["err_sq"] for p in parts) / max(sum(p["ref_sq"] for p in parts), 1e-300))),
+        "lse_max": max(p["lse_max"] for p in parts),
+        "finite": all(p["finite"] for p in parts),
+        "workers": n,
+    }
+    assert err["rows_checked"] == err["rows_total"], err
+    assert err["finite"], err
+    assert err["o_max"] <= TOL_O_MAX, err
+    assert err["o_fro"] <= TOL_O_FRO, err
+    assert err["lse_max"] <= TOL_LSE_MAX, err
+    if two_x_rule:
+        err["naive_o_max"] = max(p["naive_o_max"] for p in parts)
+        assert err["o_max"] <= 2 * err["naive_o_max"], err
+    return err
