@@ -107,7 +107,9 @@ fa_status_t launch(const void* Q, const void* K, const void* V, void* O, float* 
   p.H = H;
   p.H_kv = H_kv;
   p.n_kv_blocks = (N_kv + C::kBN - 1) / C::kBN;
-  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  // scale < 0: the tensor core forms -S and the kernel runs with |scale|.
+  p.scale_log2 = static_cast<float>(std::fabs(static_cast<double>(scale)) * 1.4426950408889634074);
+  p.idesc_qk = C::kIdescQK | (scale < 0.f ? fa::ptx::kIdescNegateA : 0u);
   p.timeout_ns = timeout_ns;
   p.drop_load = drop_load;
 
@@ -126,7 +128,6 @@ fa_status_t fwd_impl(const void* Q, const void* K, const void* V, void* O, float
   if (static_cast<long long>(B) * H * N >= (1LL << 31)) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if (scale < 0.f) return FA_ERR_UNSUPPORTED;
   for (const void* ptr : {Q, K, V, static_cast<const void*>(O)})
     if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return FA_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(LSE) % 4 != 0) return FA_ERR_INVALID_ARG;
@@ -224,7 +225,6 @@ fa_status_t check_args(const void* Q, const void* K, const void* V, const void* 
   if (static_cast<long long>(B) * H * N >= (1LL << 31)) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if (scale < 0.f) return FA_ERR_UNSUPPORTED;
   for (const void* ptr : {Q, K, V, O})
     if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return FA_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(LSE) % 4 != 0) return FA_ERR_INVALID_ARG;
@@ -391,7 +391,6 @@ fa_status_t host_impl(const void* Qh, const void* Kh, const void* Vh, void* Oh, 
   if (static_cast<long long>(B) * H * N >= (1LL << 31)) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if (scale < 0.f) return FA_ERR_UNSUPPORTED;
   const size_t need = host_workspace_bytes(B, H, N, d);
   if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256 != 0 || workspace_bytes < need)
     return FA_ERR_INVALID_ARG;
@@ -684,7 +683,6 @@ fa_status_t kv_check(const void* Q, const void* K, const void* V, const void* O,
     return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if (scale < 0.f) return FA_ERR_UNSUPPORTED;
   for (const void* ptr : {Q, K, V, O})
     if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return FA_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(LSE) % 4 != 0) return FA_ERR_INVALID_ARG;
@@ -752,7 +750,9 @@ fa_status_t decode_launch(const void* Q, const void* K, const void* V, void* O, 
   p.n_kv_blocks = k.n_kv_blocks;
   p.blocks_per_split = k.blocks_per_split;
   p.num_splits = k.num_splits;
-  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  // scale < 0: the tensor core forms -S and the kernel runs with |scale|.
+  p.scale_log2 = static_cast<float>(std::fabs(static_cast<double>(scale)) * 1.4426950408889634074);
+  p.idesc_qk = C::kIdescQK | (scale < 0.f ? fa::ptx::kIdescNegateA : 0u);
   p.timeout_ns = timeout_ns;
   p.drop_load = drop_load;
   const dim3 grid(static_cast<unsigned>(k.tiles_per_group * k.num_splits), H_kv, B);

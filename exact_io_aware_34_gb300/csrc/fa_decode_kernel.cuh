@@ -74,7 +74,8 @@ struct DecParams {
   int n_kv_blocks;
   int blocks_per_split;
   int num_splits;
-  float scale_log2;
+  float scale_log2;            // |scale| * log2(e)
+  uint32_t idesc_qk;           // instruction descriptor of S = Q K^T (A negated when scale < 0)
   unsigned long long timeout_ns;
   int drop_load;          // test hook: index of a K/V load (within a CTA's range) to skip, -1 = none
 };
@@ -221,10 +222,10 @@ __global__ void __launch_bounds__(DecCfg<HD>::kThreads, DecCfg<HD>::kCtasPerSm)
         const uint64_t a_desc = ptx::desc_kmajor_sw128(sQ), b_desc = ptx::desc_kmajor_sw128(k_tile);
         if constexpr (HD == 128)
           ptx::mma_ss_k128_warp(tmem_base + C::kColS, ptx::desc_lo(a_desc), ptx::desc_lo(b_desc),
-                                ptx::desc_hi(a_desc), C::kIdescQK, 0u);
+                                ptx::desc_hi(a_desc), p.idesc_qk, 0u);
         else
           ptx::mma_ss_k64_warp(tmem_base + C::kColS, ptx::desc_lo(a_desc), ptx::desc_lo(b_desc),
-                               ptx::desc_hi(a_desc), C::kIdescQK, 0u);
+                               ptx::desc_hi(a_desc), p.idesc_qk, 0u);
         ptx::mma_commit_warp(ptx::smem_u32(&bar_s_full));
         ptx::mma_commit_warp(ptx::smem_u32(&bar_kv_empty[(2 * jj) % C::kStages]));
       }

@@ -17,6 +17,11 @@
 //   O = O * e^{scale(m - m_new)} + P V_j          (steps 3-5, numerator form)
 // and after the last block O /= l, LSE = scale*m + ln l.
 //
+// A negative scale: the tensor core forms -S (the A operand negated through
+// the instruction descriptor) and the kernel runs with |scale|, since
+// scale * S = |scale| * (-S); the maximum the softmax keeps is then that of
+// the scaled scores, as it is for scale >= 0.
+//
 // Exactness-preserving deviation: the running maximum used for the
 // exponentials is only moved when the new row maximum exceeds it by more
 // than kRescaleLog2 (in log2 units of the scaled score). Until then the
@@ -82,7 +87,8 @@ struct FwdParams {
   int H;                       // query heads
   int H_kv;                    // K/V heads; query head h reads K/V head h / (H / H_kv)
   int n_kv_blocks;
-  float scale_log2;            // scale * log2(e)
+  float scale_log2;            // |scale| * log2(e)
+  uint32_t idesc_qk;           // instruction descriptor of S = Q K^T (A negated when scale < 0)
   unsigned long long timeout_ns;
   int drop_load;               // test hook: index of a K/V load to skip, -1 = none
 };
@@ -282,9 +288,9 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
       const uint32_t d_tmem = tmem_base + C::kColS + 128 * t;
       const uint64_t a_desc = ptx::desc_kmajor_sw128(q_tile), b_desc = ptx::desc_kmajor_sw128(k_tile);
       if constexpr (HD == 128)
-        ptx::mma_ss_k128_warp(d_tmem, ptx::desc_lo(a_desc), ptx::desc_lo(b_desc), ptx::desc_hi(a_desc), C::kIdescQK, 0u);
+        ptx::mma_ss_k128_warp(d_tmem, ptx::desc_lo(a_desc), ptx::desc_lo(b_desc), ptx::desc_hi(a_desc), p.idesc_qk, 0u);
       else
-        ptx::mma_ss_k64_warp(d_tmem, ptx::desc_lo(a_desc), ptx::desc_lo(b_desc), ptx::desc_hi(a_desc), C::kIdescQK, 0u);
+        ptx::mma_ss_k64_warp(d_tmem, ptx::desc_lo(a_desc), ptx::desc_lo(b_desc), ptx::desc_hi(a_desc), p.idesc_qk, 0u);
     };
     // K_0 is waited for here; every later K_{j+1} and V_j is waited for by
     // the softmax warps before their hand-off for block j (p_full), so the

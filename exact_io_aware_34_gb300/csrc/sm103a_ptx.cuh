@@ -196,6 +196,10 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Bit 13 of the kind::f16 instruction descriptor negates A: the product is
+// then (-A) B^T, exact for floating-point operands.
+constexpr uint32_t kIdescNegateA = 1u << 13;
+
 // ---------------------------------------------------------------- tcgen05.mma
 // D[tmem] (+)= A[smem] * B[smem]^T ; accumulate when `accum` != 0.
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,

@@ -35,7 +35,8 @@
  *     timeout (a pipeline wait that did not finish within its limit, which a
  *     correct build never hits) is reported later by fa_get_device_status.
  *   - Supported: d in {64, 128}; B, H, N >= 1 with B <= 65535, H <= 65535,
- *     B*H*N < 2^31; scale finite and >= 0; non-causal (no mask).
+ *     B*H*N < 2^31; scale finite, of either sign (zero gives uniform
+ *     weights); non-causal (no mask).
  *   - Pointers: Q, K, V, O must be 16-byte aligned, LSE 4-byte aligned. O and
  *     LSE must not overlap Q, K, V or each other.
  */
@@ -52,7 +53,7 @@ extern "C" {
 typedef enum {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = 1,  /* null or misaligned pointer, bad size, non-finite scale, overlap */
-  FA_ERR_UNSUPPORTED = 2,  /* a valid request this build does not implement (d, negative scale) */
+  FA_ERR_UNSUPPORTED = 2,  /* a valid request this build does not implement (d, a grid limit) */
   FA_ERR_CUDA = 3,         /* a CUDA runtime or driver call failed; see fa_last_cuda_error() */
   FA_ERR_TIMEOUT = 4       /* a device-side pipeline wait ran out of time (reported after the fact) */
 } fa_status_t;
@@ -114,7 +115,9 @@ fa_status_t fa_fwd_host(const void* Qh, const void* Kh, const void* Vh, void* Oh
  * {role (forward: 1 producer, 2 mma, 3 softmax/epilogue; backward dQ CTA:
  * 4, 5, 6; backward dK/dV CTA: 7, 8, 9; short-query kernel of fa_fwd_kv:
  * 10, 11, 12, in the same order), blockIdx.x, blockIdx.y,
- * blockIdx.z}; all zero when there was none.
+ * blockIdx.z}; all zero when there was none. (`info` is this library's
+ * addition for diagnosing a timeout; with info = NULL the call only reports
+ * the status.)
  */
 fa_status_t fa_get_device_status(cudaStream_t stream, unsigned int* info);
 

@@ -76,7 +76,6 @@ def call(lib, Q=A, K=A + GAP, V=A + 2 * GAP, O=A + 3 * GAP, L=A + 4 * GAP, B=1, 
     (dict(d=256), fa.FA_ERR_UNSUPPORTED),
     (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
     (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
-    (dict(scale=-0.5), fa.FA_ERR_UNSUPPORTED),
     (dict(Q=A + 8), fa.FA_ERR_INVALID_ARG),                     # not 16-byte aligned
     (dict(O=A + 3 * GAP + 4), fa.FA_ERR_INVALID_ARG),
     (dict(L=A + 4 * GAP + 2), fa.FA_ERR_INVALID_ARG),
@@ -176,7 +175,6 @@ def test_bwd_workspace_size(lib):
     (dict(ws=A + 8 * GAP), fa.FA_ERR_INVALID_ARG),               # workspace overlaps dV
     (dict(ws=A + 3 * GAP), fa.FA_ERR_INVALID_ARG),               # workspace overlaps O
     (dict(d=96), fa.FA_ERR_UNSUPPORTED),
-    (dict(scale=-1.0), fa.FA_ERR_UNSUPPORTED),
     (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
     (dict(N=0), fa.FA_ERR_INVALID_ARG),
     # 2 * B * H CTAs, past the 1-D grid limit (inputs spaced 1 TiB apart, so
@@ -230,7 +228,6 @@ def test_kv_long_query_routing(lib):
     (dict(Nq=0), fa.FA_ERR_INVALID_ARG),
     (dict(Nkv=0), fa.FA_ERR_INVALID_ARG),
     (dict(d=96), fa.FA_ERR_UNSUPPORTED),
-    (dict(scale=-1.0), fa.FA_ERR_UNSUPPORTED),
     (dict(ws=0), fa.FA_ERR_INVALID_ARG),                         # 4 splits need a workspace
     (dict(ws=A + 5 * GAP + 16), fa.FA_ERR_INVALID_ARG),          # not 128-byte aligned
     (dict(ws_bytes=4 * 8 * 129 * 4 - 1), fa.FA_ERR_INVALID_ARG),  # too small
@@ -284,7 +281,6 @@ def test_host_workspace_bytes(lib):
     (dict(N=0), fa.FA_ERR_INVALID_ARG),
     (dict(chunks=-1), fa.FA_ERR_INVALID_ARG),
     (dict(d=96), fa.FA_ERR_UNSUPPORTED),
-    (dict(scale=-1.0), fa.FA_ERR_UNSUPPORTED),
     (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
     (dict(ws=0), fa.FA_ERR_INVALID_ARG),                                   # no workspace
     (dict(ws=A + 5 * GAP + 128), fa.FA_ERR_INVALID_ARG),                   # not 256-byte aligned

@@ -147,3 +147,14 @@ def test_bwd_small_workspace_rejected():
     ws = torch.empty(fa.fa_bwd_workspace_bytes(1, 1, 256) - 16, dtype=torch.uint8, device="cuda")
     with pytest.raises(fa.FaError):
         fa.fa_bwd(q, k, v, o, torch.zeros_like(q), lse, workspace=ws)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_negative_scale(d):
+    """scale < 0: P = exp(scale Q K^T - LSE) and the scale factors of dQ and dK
+    carry the sign."""
+    q, k, v = inputs.make_random(1, 3, 500, d, seed=90 + d)
+    do = inputs.make_grad(1, 3, 500, d, seed=90 + d)
+    err, got = parity.check_bwd_full(q, k, v, do, -1 / math.sqrt(d))
+    _column_sum_properties(got[1], got[2], do)
+    print(d, err)

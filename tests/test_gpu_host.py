@@ -139,3 +139,12 @@ def test_concurrent_calls_from_two_threads():
         for oh, lh in results[i]:
             assert bits_equal(oh, od)
             assert torch.equal(lh, ld)
+
+
+def test_host_path_negative_scale():
+    """scale < 0 through the host-buffer entry point: the same bits as fa_fwd."""
+    q, k, v = inputs.make_random(1, 4, 600, 128, seed=81)
+    oh, lh = run_host(q, k, v, -0.1, num_chunks=2)
+    od, ld = parity.run_gpu(q, k, v, -0.1)
+    assert bits_equal(oh, od)
+    assert torch.equal(lh, ld)

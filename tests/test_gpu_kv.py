@@ -187,3 +187,12 @@ def test_sequence_split_emulated_on_one_gpu(world):
     assert err["finite"] and err["o_max"] <= parity.TOL_O_MAX and err["o_fro"] <= parity.TOL_O_FRO, err
     assert err["lse_max"] <= parity.TOL_LSE_MAX, err
     print(world, err)
+
+
+@pytest.mark.parametrize("N_q,N_kv,splits", [(1, 1000, 0), (16, 4096, 3), (300, 700, 1), (300, 5000, 0)])
+def test_negative_scale(N_q, N_kv, splits):
+    """scale < 0 on both kernels of fa_fwd_kv (short queries with a key split,
+    and the fused kernel for long query blocks)."""
+    q, k, v = inputs.make_kv(1, 8, 2, N_q, N_kv, 128, seed=60 + N_q)
+    err, _, _ = check_kv(q, k, v, -0.11, num_splits=splits)
+    print(N_q, N_kv, splits, err)

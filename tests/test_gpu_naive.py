@@ -75,3 +75,22 @@ def test_naive_rejects_small_workspace():
     with pytest.raises(fa.FaError) as ei:
         fa.fa_naive_fwd(q, q.clone(), q.clone(), workspace=ws)
     assert ei.value.status == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_naive_negative_scale(d):
+    """scale < 0: the comparator's scores are bf16(scale * bf16(Q K^T)) with the
+    sign carried through; the result is attention with the materialise path's
+    accuracy."""
+    q, k, v = inputs.make_random(1, 3, 400, d, seed=70 + d)
+    s = -1 / math.sqrt(d)
+    o, lse = fa.fa_naive_fwd(q.cuda(), k.cuda(), v.cuda(), scale=s)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status()[0] == fa.FA_OK
+    Q, K, V = (parity.to64(x) for x in (q, k, v))
+    On = oracle.naive_bf16_attention(Q, K, V, s)
+    O_ref, _ = oracle.attention(Q, K, V, s)
+    og = parity.to64(o.cpu())
+    assert np.abs(og - On).max() <= 1e-2
+    assert np.abs(og - O_ref).max() <= 1.5 * np.abs(On - O_ref).max() + 2e-3
+    assert np.abs(parity.to64(lse.cpu()) - emulated_lse(Q, K, s)).max() <= 5e-3

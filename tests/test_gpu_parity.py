@@ -200,3 +200,25 @@ def test_lse_rebuilds_probabilities():
     S = s * (parity.to64(q) @ np.swapaxes(parity.to64(k), -1, -2))
     rows = np.exp(S - parity.to64(lse)[..., None]).sum(-1)
     assert np.abs(rows - 1).max() < 2e-3
+
+
+# --- negative scale ----------------------------------------------------------------
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("scale", [-0.1, -0.125, -1.5])
+def test_negative_scale(d, scale):
+    """scale < 0 puts the most weight on the keys least aligned with each query;
+    the kernel has the tensor core form -S and runs with |scale|."""
+    q, k, v = inputs.make_random(2, 3, 700, d, seed=20 + d)
+    err, _, _ = parity.check_full(q, k, v, scale, two_x_rule=abs(scale) <= 0.2)
+    print(d, scale, err)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_negative_scale_equals_negated_keys(d):
+    """scale * Q K^T = |scale| * Q (-K)^T: negating the scale or the keys gives
+    the same scores (negation is exact), so the two calls agree bit for bit."""
+    q, k, v = inputs.make_random(1, 2, 513, d, seed=23 + d)
+    o1, l1 = parity.run_gpu(q, k, v, -0.09)
+    o2, l2 = parity.run_gpu(q, -k, v, 0.09)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1, l2)
