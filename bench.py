@@ -20,6 +20,11 @@ shape with shared K/V heads (fa_fwd_kv: B=4, 32 query heads on 8 K/V heads,
 one query row against 32768 keys, d=128) under "decode" in K/V GB/s against
 the HBM roofline (skip with --no-decode).
 
+The other four workloads of the same family (N=256 d=64; B=4 H=16 N=1024
+d=64; B=2 H=16 N=4096 d=128; the spiky N=32768 d=128 shape) are timed the same
+way and reported under "per_config", each with its roofline fraction, clocks
+and the CPU oracle on a row sample beside it (skip with --no-per-config).
+
 --impl reference times the CPU oracle (float64, numpy) on the host cores, on a
 bounded sample of the same workload per step.
 """
@@ -462,6 +467,28 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------------------- native arm
+def time_forward(fa, qd, kd, vd, o, lse, scale, flush, stream, steps, warmup, local, uuid):
+    """``steps`` fa_fwd calls, each bracketed by CUDA events on ``stream`` with the
+    L2 cache flushed before it (outside the events); returns (per-step ms, clocks)."""
+    import torch
+    for _ in range(warmup):
+        fa.fa_fwd(qd, kd, vd, o, lse, scale)
+    torch.cuda.synchronize(qd.device)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    with ClockSampler(local, uuid) as clocks:
+        for i in range(steps):
+            flush.fill_(float(i))
+            starts[i].record(stream)
+            fa.fa_fwd(qd, kd, vd, o, lse, scale)
+            ends[i].record(stream)
+        torch.cuda.synchronize(qd.device)
+    st, info = fa.fa_get_device_status()
+    if st != fa.FA_OK:
+        raise RuntimeError(f"device status after timed forward steps: {fa.fa_status_string(st)} {info}")
+    return [a.elapsed_time(b) for a, b in zip(starts, ends)], clocks.summary()
+
+
 def run_native(args):
     import torch
     world, rank, local = dist_setup()
@@ -481,6 +508,12 @@ def run_native(args):
             cpu_bwd = cpu_baseline_bwd(args.workload, target_s=min(10.0, args.cpu_seconds))
         if not args.no_decode:
             cpu_dec = cpu_baseline_decode(DECODE_WORKLOAD)
+    cpu_cfg = {}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.no_per_config:
+        from exact_io_aware_34_gb300 import inputs as _inp
+        for cw in _inp.WORKLOADS:
+            if cw.name != args.workload:
+                cpu_cfg[cw.name] = cpu_baseline(cw.name, target_s=args.cfg_cpu_seconds)
 
     from exact_io_aware_34_gb300 import build as fa_build
     from exact_io_aware_34_gb300 import fa, inputs
@@ -525,6 +558,44 @@ def run_native(args):
     st, info = fa.fa_get_device_status()
     if st != fa.FA_OK:
         raise RuntimeError(f"device status after timed steps: {fa.fa_status_string(st)} {info}")
+
+    # The other workloads of the family, timed the same way (their own inputs,
+    # flushed L2 before every step, clocks sampled during the timed steps).
+    per_config = []
+    if not args.no_per_config:
+        peaks_pc, peak_src_pc = load_peaks()
+        for cw in inputs.WORKLOADS:
+            if cw.name == w.name:
+                continue
+            cq, ck, cv, cs = inputs.make_inputs(cw)
+            cqd, ckd, cvd = (x.to(device) for x in (cq, ck, cv))
+            co = torch.empty_like(cqd)
+            cl = torch.empty(cqd.shape[:3], dtype=torch.float32, device=device)
+            n_steps = max(3, min(args.steps, 20))
+            c_ms, c_clk = time_forward(fa, cqd, ckd, cvd, co, cl, cs, flush, stream, n_steps, args.warmup, local,
+                                       uuid)
+            c_avg = sum(c_ms) / len(c_ms)
+            c_val = cw.flops / (c_avg * 1e-3) / 1e12
+            entry = {
+                "workload": cw.name, "config": cw.describe(), "value": c_val, "unit": UNIT, "steps": n_steps,
+                "ms_per_step": c_avg,
+                "step_ms": {"min": min(c_ms), "median": statistics.median(c_ms), "max": max(c_ms)},
+                "roofline": {"bound": "tensor", "achieved": c_val, "peak": peaks_pc["bf16_tflops"], "unit": UNIT,
+                             "frac": c_val / peaks_pc["bf16_tflops"],
+                             "frac_of_sustained": c_val / peaks_pc["bf16_tflops_sustained"],
+                             "peak_source": f"{peak_src_pc} dense bf16 burst",
+                             "traffic": load_traffic(cw.name),
+                             "kernel": f"fa_fwd_kernel<{cw.d}>", "flops_per_launch": cw.flops,
+                             "algorithmic_bytes_per_launch": cw.B * cw.H * cw.N * (8 * cw.d + 4)},
+                "gpu_launches": n_steps,
+                "l2": "flushed before every step (512 MB write, outside the events)",
+                "clocks": c_clk,
+            }
+            if cw.name in cpu_cfg:
+                entry["cpu_baseline"] = cpu_cfg[cw.name]
+            per_config.append(entry)
+            del cqd, ckd, cvd, co, cl
+        torch.cuda.empty_cache()
 
     # The standard-attention comparator on the same inputs: S and P in HBM
     # ("01 · 注意力为什么是 IO 瓶颈" §3), same timing rules as the fused steps.
@@ -717,6 +788,8 @@ def run_native(args):
             if cpu_dec is not None:
                 decode["cpu_baseline"] = cpu_dec
             line["decode"] = decode
+        if per_config:
+            line["per_config"] = per_config
         if cpu is not None:
             line["cpu_baseline"] = cpu
         if cpu_small:
@@ -741,6 +814,9 @@ def main(argv=None):
     ap.add_argument("--no-comparator", action="store_true", help="skip timing standard attention (S/P in HBM)")
     ap.add_argument("--no-bwd", action="store_true", help="skip timing the backward pass")
     ap.add_argument("--no-decode", action="store_true", help="skip timing the shared-K/V-head decode shape")
+    ap.add_argument("--no-per-config", action="store_true", help="skip timing the other four forward workloads")
+    ap.add_argument("--cfg-cpu-seconds", type=float, default=4.0,
+                    help="CPU oracle sample size for each of the other workloads (seconds of work)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

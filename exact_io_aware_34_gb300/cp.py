@@ -9,9 +9,11 @@ fit one device. The exchange step is the one the online softmax allows
   2. the ranks all-gather the partial results (one collective per output);
   3. each rank merges them, LSE = ln sum_r e^{LSE_r} and
      O = sum_r e^{LSE_r - LSE} O_r, into the attention over all keys.
-Step 1 is fa_fwd_kv and step 3 fa_merge_partials, both CUDA kernels of this
-library; step 2 is torch.distributed (NCCL between GPUs). Nothing here
-touches the data outside those calls.
+Step 1 is fa_fwd_kv_f32 (O stays float32, so the exchange carries it
+unrounded) and step 3 fa_merge_partials (which rounds O to bf16 once), both
+CUDA kernels of this library; step 2 is torch.distributed: NCCL between GPUs,
+or gloo, which gathers through host copies of the partial results. Nothing
+here touches the data outside those calls.
 """
 from __future__ import annotations
 
@@ -42,7 +44,7 @@ def shard_bounds(n_kv: int, world: int, rank: int):
 
 def _partial_cuda(q, k, v, scale):
     from . import fa
-    return fa.fa_fwd_kv(q, k, v, scale=scale)
+    return fa.fa_fwd_kv_f32(q, k, v, scale=scale)
 
 
 def _merge_cuda(o_parts, lse_parts):
@@ -65,10 +67,19 @@ def fa_fwd_cp(q, k_shard, v_shard, scale: float | None = None, group=None, parti
         scale = 1.0 / math.sqrt(q.shape[-1])
     world = dist.get_world_size(group)
     o_r, lse_r = (partial_fn or _partial_cuda)(q, k_shard, v_shard, scale)
-    o32 = o_r.float().contiguous()
-    lse_r = lse_r.contiguous()
-    o_list = [torch.empty_like(o32) for _ in range(world)]
+    if o_r.dtype != torch.float32 and o_r.dtype != torch.float64:
+        raise TypeError(f"partial O must stay float32 for the exchange, got {o_r.dtype}")
+    o_r, lse_r = o_r.contiguous(), lse_r.contiguous()
+    device = o_r.device
+    # gloo gathers host tensors only: the partial results cross through host memory.
+    via_host = device.type == "cuda" and dist.get_backend(group) == "gloo"
+    if via_host:
+        o_r, lse_r = o_r.cpu(), lse_r.cpu()
+    o_list = [torch.empty_like(o_r) for _ in range(world)]
     l_list = [torch.empty_like(lse_r) for _ in range(world)]
-    dist.all_gather(o_list, o32, group=group)
+    dist.all_gather(o_list, o_r, group=group)
     dist.all_gather(l_list, lse_r, group=group)
-    return (merge_fn or _merge_cuda)(torch.stack(o_list), torch.stack(l_list))
+    o_parts, l_parts = torch.stack(o_list), torch.stack(l_list)
+    if via_host:
+        o_parts, l_parts = o_parts.to(device), l_parts.to(device)
+    return (merge_fn or _merge_cuda)(o_parts, l_parts)

@@ -675,7 +675,7 @@ size_t kv_workspace_bytes(int B, int H, int N_q, int d, const KvPlan& k) {
 }
 
 fa_status_t kv_check(const void* Q, const void* K, const void* V, const void* O, const float* LSE, int B, int H,
-                     int H_kv, int N_q, int N_kv, int d, float scale) {
+                     int H_kv, int N_q, int N_kv, int d, float scale, size_t o_elem_bytes) {
   if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || H_kv < 1 || N_q < 1 || N_kv < 1 || d < 1) return FA_ERR_INVALID_ARG;
   if (B > 65535 || H > 65535 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
@@ -687,18 +687,19 @@ fa_status_t kv_check(const void* Q, const void* K, const void* V, const void* O,
     if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return FA_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(LSE) % 4 != 0) return FA_ERR_INVALID_ARG;
   const size_t n_q = static_cast<size_t>(B) * H * N_q * d * 2;
+  const size_t n_o = static_cast<size_t>(B) * H * N_q * d * o_elem_bytes;
   const size_t n_kv = static_cast<size_t>(B) * H_kv * N_kv * d * 2;
   const size_t n_lse = static_cast<size_t>(B) * H * N_q * 4;
-  if (overlaps(O, n_q, Q, n_q) || overlaps(O, n_q, K, n_kv) || overlaps(O, n_q, V, n_kv)) return FA_ERR_INVALID_ARG;
+  if (overlaps(O, n_o, Q, n_q) || overlaps(O, n_o, K, n_kv) || overlaps(O, n_o, V, n_kv)) return FA_ERR_INVALID_ARG;
   if (overlaps(LSE, n_lse, Q, n_q) || overlaps(LSE, n_lse, K, n_kv) || overlaps(LSE, n_lse, V, n_kv) ||
-      overlaps(LSE, n_lse, O, n_q))
+      overlaps(LSE, n_lse, O, n_o))
     return FA_ERR_INVALID_ARG;
   return FA_OK;
 }
 
 template <int HD>
 fa_status_t decode_launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int H_kv,
-                          int N_q, int N_kv, float scale, const KvPlan& k, void* ws, int drop_load,
+                          int N_q, int N_kv, float scale, const KvPlan& k, void* ws, bool f32_out, int drop_load,
                           unsigned long long timeout_ns, cudaStream_t stream) {
   using C = fa::DecCfg<HD>;
   int dev = 0;
@@ -734,10 +735,17 @@ fa_status_t decode_launch(const void* Q, const void* K, const void* V, void* O, 
 
   fa::DecParams p;
   const size_t rows = static_cast<size_t>(B) * H * N_q;
-  p.O = static_cast<__nv_bfloat16*>(O);
+  p.O = f32_out ? nullptr : static_cast<__nv_bfloat16*>(O);
   p.LSE = LSE;
-  p.O_part = k.num_splits > 1 ? static_cast<float*>(ws) : nullptr;
-  p.LSE_part = k.num_splits > 1 ? static_cast<float*>(ws) + static_cast<size_t>(k.num_splits) * rows * HD : nullptr;
+  p.f32_out = f32_out ? 1 : 0;
+  if (k.num_splits > 1) {
+    p.O_part = static_cast<float*>(ws);
+    p.LSE_part = static_cast<float*>(ws) + static_cast<size_t>(k.num_splits) * rows * HD;
+  } else {
+    // One split with float32 results: the kernel's partial result is the result.
+    p.O_part = f32_out ? static_cast<float*>(O) : nullptr;
+    p.LSE_part = f32_out ? LSE : nullptr;
+  }
   p.N_q = N_q;
   p.N_kv = N_kv;
   p.H = H;
@@ -772,9 +780,14 @@ fa_status_t decode_launch(const void* Q, const void* K, const void* V, void* O, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, fa::decode_merge_kernel<HD>, static_cast<const float*>(p.O_part),
-                           static_cast<const float*>(p.LSE_part), static_cast<__nv_bfloat16*>(O), LSE,
-                           static_cast<long long>(rows), k.num_splits);
+    if (f32_out)
+      e = cudaLaunchKernelEx(&cfg, fa::decode_merge_kernel<HD, float>, static_cast<const float*>(p.O_part),
+                             static_cast<const float*>(p.LSE_part), static_cast<float*>(O), LSE,
+                             static_cast<long long>(rows), k.num_splits);
+    else
+      e = cudaLaunchKernelEx(&cfg, fa::decode_merge_kernel<HD>, static_cast<const float*>(p.O_part),
+                             static_cast<const float*>(p.LSE_part), static_cast<__nv_bfloat16*>(O), LSE,
+                             static_cast<long long>(rows), k.num_splits);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   return FA_OK;
@@ -782,10 +795,13 @@ fa_status_t decode_launch(const void* Q, const void* K, const void* V, void* O, 
 
 fa_status_t kv_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int H_kv,
                     int N_q, int N_kv, int d, float scale, int num_splits, void* workspace, size_t workspace_bytes,
-                    int drop_load, unsigned long long timeout_ns, cudaStream_t stream) {
-  fa_status_t st = kv_check(Q, K, V, O, LSE, B, H, H_kv, N_q, N_kv, d, scale);
+                    bool f32_out, int drop_load, unsigned long long timeout_ns, cudaStream_t stream) {
+  fa_status_t st = kv_check(Q, K, V, O, LSE, B, H, H_kv, N_q, N_kv, d, scale, f32_out ? 4 : 2);
   if (st != FA_OK) return st;
-  const KvRoute route = kv_route(B, H, H_kv, N_q, N_kv, num_splits);
+  // Float32 results come from the short-query kernel (the fused kernel
+  // writes bf16).
+  const KvRoute route =
+      f32_out ? KvRoute{false, kv_plan(B, H, H_kv, N_q, N_kv, num_splits)} : kv_route(B, H, H_kv, N_q, N_kv, num_splits);
   if (route.fused) {
     // Long query blocks: the fused forward kernel with the K/V head mapping.
     if (d == 64) return launch<64>(Q, K, V, O, LSE, B, H, H_kv, N_q, N_kv, scale, drop_load, timeout_ns, stream);
@@ -798,17 +814,18 @@ fa_status_t kv_impl(const void* Q, const void* K, const void* V, void* O, float*
     if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 128 != 0 || workspace_bytes < need)
       return FA_ERR_INVALID_ARG;
     const size_t n_q = static_cast<size_t>(B) * H * N_q * d * 2;
+    const size_t n_o = static_cast<size_t>(B) * H * N_q * d * (f32_out ? 4 : 2);
     const size_t n_kv = static_cast<size_t>(B) * H_kv * N_kv * d * 2;
     if (overlaps(workspace, need, Q, n_q) || overlaps(workspace, need, K, n_kv) ||
-        overlaps(workspace, need, V, n_kv) || overlaps(workspace, need, O, n_q) ||
+        overlaps(workspace, need, V, n_kv) || overlaps(workspace, need, O, n_o) ||
         overlaps(workspace, need, LSE, static_cast<size_t>(B) * H * N_q * 4))
       return FA_ERR_INVALID_ARG;
   }
   if (d == 64)
-    return decode_launch<64>(Q, K, V, O, LSE, B, H, H_kv, N_q, N_kv, scale, k, workspace, drop_load, timeout_ns,
-                             stream);
-  return decode_launch<128>(Q, K, V, O, LSE, B, H, H_kv, N_q, N_kv, scale, k, workspace, drop_load, timeout_ns,
-                            stream);
+    return decode_launch<64>(Q, K, V, O, LSE, B, H, H_kv, N_q, N_kv, scale, k, workspace, f32_out, drop_load,
+                             timeout_ns, stream);
+  return decode_launch<128>(Q, K, V, O, LSE, B, H, H_kv, N_q, N_kv, scale, k, workspace, f32_out, drop_load,
+                            timeout_ns, stream);
 }
 
 }  // namespace
@@ -830,7 +847,19 @@ size_t fa_fwd_kv_workspace_bytes(int B, int H, int H_kv, int N_q, int N_kv, int 
 fa_status_t fa_fwd_kv(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int H_kv,
                       int N_q, int N_kv, int d, float scale, int num_splits, void* workspace, size_t workspace_bytes,
                       cudaStream_t stream) {
-  return kv_impl(Q, K, V, O, LSE, B, H, H_kv, N_q, N_kv, d, scale, num_splits, workspace, workspace_bytes, -1,
+  return kv_impl(Q, K, V, O, LSE, B, H, H_kv, N_q, N_kv, d, scale, num_splits, workspace, workspace_bytes, false, -1,
+                 kDefaultTimeoutNs, stream);
+}
+
+size_t fa_fwd_kv_f32_workspace_bytes(int B, int H, int H_kv, int N_q, int N_kv, int d, int num_splits) {
+  if (B < 1 || H < 1 || H_kv < 1 || H % H_kv != 0 || N_q < 1 || N_kv < 1 || (d != 64 && d != 128)) return 0;
+  return kv_workspace_bytes(B, H, N_q, d, kv_plan(B, H, H_kv, N_q, N_kv, num_splits));
+}
+
+fa_status_t fa_fwd_kv_f32(const void* Q, const void* K, const void* V, float* O, float* LSE, int B, int H, int H_kv,
+                          int N_q, int N_kv, int d, float scale, int num_splits, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream) {
+  return kv_impl(Q, K, V, O, LSE, B, H, H_kv, N_q, N_kv, d, scale, num_splits, workspace, workspace_bytes, true, -1,
                  kDefaultTimeoutNs, stream);
 }
 
@@ -839,7 +868,7 @@ fa_status_t fa_fwd_kv_fault_test(const void* Q, const void* K, const void* V, vo
                                  size_t workspace_bytes, int drop_load, unsigned long long timeout_ns,
                                  cudaStream_t stream) {
   if (timeout_ns == 0) return FA_ERR_INVALID_ARG;
-  return kv_impl(Q, K, V, O, LSE, B, H, H_kv, N_q, N_kv, d, scale, num_splits, workspace, workspace_bytes,
+  return kv_impl(Q, K, V, O, LSE, B, H, H_kv, N_q, N_kv, d, scale, num_splits, workspace, workspace_bytes, false,
                  drop_load < 0 ? -1 : drop_load, timeout_ns, stream);
 }
 

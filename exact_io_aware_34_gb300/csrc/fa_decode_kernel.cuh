@@ -58,10 +58,11 @@ struct DecCfg {
 };
 
 struct DecParams {
-  __nv_bfloat16* O;       // [B, H, N_q, d] (num_splits == 1)
-  float* LSE;             // [B, H, N_q]    (num_splits == 1)
-  float* O_part;          // [num_splits][B*H*N_q][d] (num_splits > 1)
+  __nv_bfloat16* O;       // [B, H, N_q, d] (num_splits == 1 and !f32_out)
+  float* LSE;             // [B, H, N_q]    (num_splits == 1 and !f32_out)
+  float* O_part;          // [num_splits][B*H*N_q][d] (num_splits > 1 or f32_out)
   float* LSE_part;        // [num_splits][B*H*N_q]
+  int f32_out;            // 1: results stay float32 (normalised O and LSE) in O_part / LSE_part
   int N_q;
   int N_kv;
   int H;
@@ -369,7 +370,7 @@ __global__ void __launch_bounds__(DecCfg<HD>::kThreads, DecCfg<HD>::kCtasPerSm)
         ptx::tmem_ld_wait();
         ptx::reg_fence32(o);
         if (!in_range) continue;
-        if (p.num_splits == 1) {
+        if (p.num_splits == 1 && !p.f32_out) {
           uint32_t packed[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i)
@@ -387,7 +388,7 @@ __global__ void __launch_bounds__(DecCfg<HD>::kThreads, DecCfg<HD>::kCtasPerSm)
         }
       }
       if (in_range) {
-        if (p.num_splits == 1) p.LSE[grow] = lse;
+        if (p.num_splits == 1 && !p.f32_out) p.LSE[grow] = lse;
         else p.LSE_part[split * n_rows + grow] = lse;
       }
     }
@@ -405,13 +406,14 @@ __global__ void __launch_bounds__(DecCfg<HD>::kThreads, DecCfg<HD>::kCtasPerSm)
 
 // One warp per query row: combine the num_splits partial results of the row.
 // LSE = m + ln sum_s e^{LSE_s - m} with m = max_s LSE_s, and
-// O = sum_s e^{LSE_s - LSE} O_s, rounded once to bf16. The splits' LSE are
+// O = sum_s e^{LSE_s - LSE} O_s, rounded once to bf16 (OutT = __nv_bfloat16)
+// or kept in float32 (OutT = float). The splits' LSE are
 // read by the lanes in parallel (32 at a time) and their weights passed by
 // shuffles, so the row costs two dependent rounds of loads, not 2 x splits.
-template <int HD>
+template <int HD, typename OutT = __nv_bfloat16>
 __global__ void __launch_bounds__(256) decode_merge_kernel(const float* __restrict__ O_part,
                                                            const float* __restrict__ LSE_part,
-                                                           __nv_bfloat16* __restrict__ O, float* __restrict__ LSE,
+                                                           OutT* __restrict__ O, float* __restrict__ LSE,
                                                            long long n_rows, int num_splits) {
   // Launched as a programmatic dependent of the decode kernel: wait here until
   // that grid has finished and its partials are visible (returns at once when
@@ -448,10 +450,16 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const float* __restri
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
   const float inv = 1.f / total;
-  __nv_bfloat16* dst = O + row * HD + lane * kPer;
+  OutT* dst = O + row * HD + lane * kPer;
+  if constexpr (sizeof(OutT) == 4) {
 #pragma unroll
-  for (int e = 0; e < kPer; e += 2)
-    *reinterpret_cast<__nv_bfloat162*>(dst + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+    for (int e = 0; e < kPer; e += 2)
+      *reinterpret_cast<float2*>(dst + e) = make_float2(acc[e] * inv, acc[e + 1] * inv);
+  } else {
+#pragma unroll
+    for (int e = 0; e < kPer; e += 2)
+      *reinterpret_cast<__nv_bfloat162*>(dst + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+  }
   if (lane == 0) LSE[row] = m + __logf(total);
 }
 

@@ -27,7 +27,8 @@ FA_ERR_TIMEOUT = 4
 EXPORTED = ("fa_fwd", "fa_get_device_status", "fa_status_string", "fa_last_cuda_error", "fa_fwd_fault_test",
             "fa_naive_fwd", "fa_naive_workspace_bytes", "fa_naive_fwd_noalloc", "fa_bwd", "fa_bwd_workspace_bytes",
             "fa_bwd_fault_test", "fa_fwd_kv", "fa_fwd_kv_num_splits", "fa_fwd_kv_workspace_bytes",
-            "fa_fwd_kv_fault_test", "fa_merge_partials", "fa_fwd_host", "fa_fwd_host_workspace_bytes")
+            "fa_fwd_kv_fault_test", "fa_merge_partials", "fa_fwd_host", "fa_fwd_host_workspace_bytes",
+            "fa_fwd_kv_f32", "fa_fwd_kv_f32_workspace_bytes")
 
 _lib = None
 
@@ -85,6 +86,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_fwd_kv_num_splits.restype = i
     lib.fa_fwd_kv_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
     lib.fa_fwd_kv_workspace_bytes.restype = ctypes.c_size_t
+    lib.fa_fwd_kv_f32.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, ctypes.c_size_t, vp]
+    lib.fa_fwd_kv_f32.restype = i
+    lib.fa_fwd_kv_f32_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
+    lib.fa_fwd_kv_f32_workspace_bytes.restype = ctypes.c_size_t
     lib.fa_merge_partials.argtypes = [vp, vp, vp, vp, i, ctypes.c_longlong, i, vp]
     lib.fa_merge_partials.restype = i
     _lib = lib
@@ -284,6 +289,43 @@ def fa_fwd_kv(q, k, v, o=None, lse=None, scale: float | None = None, num_splits:
                            N_kv, d, float(scale), int(num_splits), ws_ptr, ws_bytes, _stream_handle(stream, q.device))
     if st != FA_OK:
         raise FaError(st, "fa_fwd_kv")
+    return o, lse
+
+
+def fa_fwd_kv_f32_workspace_bytes(B: int, H: int, H_kv: int, N_q: int, N_kv: int, d: int,
+                                  num_splits: int = 0) -> int:
+    return int(load_library().fa_fwd_kv_f32_workspace_bytes(int(B), int(H), int(H_kv), int(N_q), int(N_kv), int(d),
+                                                             int(num_splits)))
+
+
+def fa_fwd_kv_f32(q, k, v, o=None, lse=None, scale: float | None = None, num_splits: int = 0, workspace=None,
+                  stream=None):
+    """:func:`fa_fwd_kv` with o returned in float32 (normalised, not rounded):
+    the partial result of one key shard that a sequence split exchanges.
+    Returns (o float32 [B, H, N_q, d], lse float32 [B, H, N_q])."""
+    _check_kv(q, k, v)
+    B, H, N_q, d = q.shape
+    H_kv, N_kv = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty((B, H, N_q, d), dtype=torch.float32, device=q.device)
+    if o.dtype != torch.float32 or tuple(o.shape) != (B, H, N_q, d) or not o.is_contiguous():
+        raise ValueError("o must be a contiguous float32 [B, H, N_q, d] tensor")
+    if lse is None:
+        lse = torch.empty((B, H, N_q), dtype=torch.float32, device=q.device)
+    need = fa_fwd_kv_f32_workspace_bytes(B, H, H_kv, N_q, N_kv, d, num_splits)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.fa_fwd_kv_f32(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, H_kv,
+                               N_q, N_kv, d, float(scale), int(num_splits), ws_ptr, ws_bytes,
+                               _stream_handle(stream, q.device))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_kv_f32")
     return o, lse
 
 

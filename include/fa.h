@@ -229,6 +229,31 @@ int fa_fwd_kv_num_splits(int B, int H, int H_kv, int N_q, int N_kv, int d);
 size_t fa_fwd_kv_workspace_bytes(int B, int H, int H_kv, int N_q, int N_kv, int d, int num_splits);
 
 /*
+ * fa_fwd_kv_f32_workspace_bytes -- workspace bytes fa_fwd_kv_f32 needs:
+ * num_splits * B*H*N_q * (d + 1) float32 partial results when the short-query
+ * kernel's key split (num_splits, 0 = automatic, as for fa_fwd_kv) has more
+ * than one range, else 0. 0 also for invalid sizes.
+ */
+size_t fa_fwd_kv_f32_workspace_bytes(int B, int H, int H_kv, int N_q, int N_kv, int d, int num_splits);
+
+/*
+ * fa_fwd_kv_f32 -- fa_fwd_kv with O kept in float32: O[r] is the softmax-
+ * weighted sum of the value rows, normalised by its own l, not rounded to
+ * bf16. This is the partial result one device of a sequence split hands to
+ * the others: the exchange carries it in float32 and only the final merge
+ * (fa_merge_partials) rounds, once ("Flash Attention (FA1)", derivation
+ * steps 4-5: partial results over disjoint key sets combine exactly).
+ *   O   : device, float32 [B, H, N_q, d], written.  LSE : float32 [B, H, N_q].
+ *   Other arguments, limits and errors as for fa_fwd_kv. Every shape runs on
+ *   the short-query kernel (128 query rows per tile); with more than one key
+ *   range a merge kernel writes O and LSE (two launches), with one the kernel
+ *   writes them itself.
+ */
+fa_status_t fa_fwd_kv_f32(const void* Q, const void* K, const void* V, float* O, float* LSE,
+                          int B, int H, int H_kv, int N_q, int N_kv, int d, float scale,
+                          int num_splits, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * fa_fwd_kv_fault_test -- TEST HOOK, not for production use. fa_fwd_kv with
  * every device-side wait limited to `timeout_ns`, and, when drop_load >= 0,
  * the drop_load-th K/V tile load skipped in every CTA (in the short-query

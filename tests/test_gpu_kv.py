@@ -168,19 +168,100 @@ def test_merge_partials_matches_oracle():
     assert float(np.abs(lse.cpu().numpy() - L_ref).max()) <= 1e-4
 
 
+# --- float32 partial results (the exchange format of a sequence split) -------------
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N_q,N_kv,splits", [(1, 1000, 0), (16, 4096, 1), (100, 777, 3), (300, 2000, 2),
+                                             (300, 2000, 1)])
+def test_kv_f32_partial_result(d, N_q, N_kv, splits):
+    """fa_fwd_kv_f32 keeps O in float32: within the parity tolerances of the
+    oracle, and, rounded to bf16, bit for bit fa_fwd_kv's O on the same kernel
+    path (the short-query kernel with the same key split)."""
+    q, k, v = inputs.make_kv(1, 8, 2, N_q, N_kv, d, seed=380 + N_q + d)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    s = 1 / math.sqrt(d)
+    o32, l32 = fa.fa_fwd_kv_f32(qd, kd, vd, scale=s, num_splits=splits)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status()[0] == fa.FA_OK
+    assert o32.dtype == torch.float32
+    O_ref, L_ref = oracle.attention_gqa(*(parity.to64(x) for x in (q, k, v)), s)
+    err = parity.errors(o32.cpu(), l32.cpu(), O_ref, L_ref)
+    assert err["finite"] and err["o_max"] <= parity.TOL_O_MAX and err["o_fro"] <= parity.TOL_O_FRO, err
+    assert err["lse_max"] <= parity.TOL_LSE_MAX, err
+    # the same kernel with bf16 output: force the short-query route for long queries
+    same_route = splits if (N_q <= 128 or splits != 1) else None
+    if same_route is not None:
+        o16, l16 = fa.fa_fwd_kv(qd, kd, vd, scale=s, num_splits=same_route)
+        torch.cuda.synchronize()
+        assert torch.equal(o32.to(torch.bfloat16).view(torch.int16), o16.view(torch.int16))
+        assert torch.equal(l32, l16)
+    print(d, N_q, N_kv, splits, err)
+
+
+def _cp_rank(rank, world, port, folder):
+    """One rank of a sequence split on the one GPU: its key shard through
+    fa_fwd_kv_f32, the gather over gloo through host copies, the merge on the
+    GPU (the library's fa_fwd_cp end to end)."""
+    import os
+    import torch.distributed as dist
+    from exact_io_aware_34_gb300 import build, cp
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    build.build()
+    fa.load_library()
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        q, k, v = inputs.make_kv(1, 8, 2, 300, 5000, 128, seed=390 + world)
+        s0, s1 = cp.shard_bounds(5000, world, rank)
+        dev = torch.device("cuda", 0)
+        o, lse = cp.fa_fwd_cp(q.to(dev), k[:, :, s0:s1].contiguous().to(dev), v[:, :, s0:s1].contiguous().to(dev),
+                              scale=0.09)
+        torch.cuda.synchronize(dev)
+        assert fa.fa_get_device_status()[0] == fa.FA_OK
+        torch.save({"o": o.cpu(), "lse": lse.cpu()}, os.path.join(folder, f"rank{rank}.pt"))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_fa_fwd_cp_across_gloo_ranks_on_one_gpu(world, tmp_path):
+    """cp.fa_fwd_cp itself, run by ``world`` processes that share the GPU (each
+    launches only its own independent kernels; nothing waits on another rank's
+    kernel): every rank's merged result equals attention over all keys."""
+    import socket
+    import torch.multiprocessing as tmp
+    from exact_io_aware_34_gb300 import cp  # noqa: F401
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    tmp.start_processes(_cp_rank, args=(world, port, str(tmp_path)), nprocs=world, start_method="spawn", join=True)
+    q, k, v = inputs.make_kv(1, 8, 2, 300, 5000, 128, seed=390 + world)
+    O_ref, L_ref = oracle.attention_gqa(parity.to64(q), parity.to64(k), parity.to64(v), 0.09)
+    first = None
+    for r in range(world):
+        res = torch.load(tmp_path / f"rank{r}.pt")
+        err = parity.errors(res["o"], res["lse"], O_ref, L_ref)
+        assert err["finite"] and err["o_max"] <= parity.TOL_O_MAX and err["o_fro"] <= parity.TOL_O_FRO, err
+        assert err["lse_max"] <= parity.TOL_LSE_MAX, err
+        if first is None:
+            first = res
+        else:   # every rank merges the same gathered partials
+            assert torch.equal(res["o"].view(torch.int16), first["o"].view(torch.int16))
+        print(world, r, err)
+
+
 @pytest.mark.parametrize("world", [2, 3, 8])
 def test_sequence_split_emulated_on_one_gpu(world):
     """The ranks of a sequence split, run one after another on one GPU: each
-    shard's partial result from fa_fwd_kv, then one fa_merge_partials call,
-    against the oracle over all keys."""
+    shard's float32 partial result from fa_fwd_kv_f32, then one
+    fa_merge_partials call, against the oracle over all keys."""
     from exact_io_aware_34_gb300 import cp
     q, k, v = inputs.make_kv(1, 8, 2, 300, 5000, 128, seed=370 + world)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     parts = []
     for r in range(world):
         s0, s1 = cp.shard_bounds(5000, world, r)
-        parts.append(fa.fa_fwd_kv(qd, kd[:, :, s0:s1].contiguous(), vd[:, :, s0:s1].contiguous(), scale=0.09))
-    o, lse = fa.fa_merge_partials(torch.stack([p[0].float() for p in parts]), torch.stack([p[1] for p in parts]))
+        parts.append(fa.fa_fwd_kv_f32(qd, kd[:, :, s0:s1].contiguous(), vd[:, :, s0:s1].contiguous(), scale=0.09))
+    o, lse = fa.fa_merge_partials(torch.stack([p[0] for p in parts]), torch.stack([p[1] for p in parts]))
     torch.cuda.synchronize()
     O_ref, L_ref = oracle.attention_gqa(parity.to64(q), parity.to64(k), parity.to64(v), 0.09)
     err = parity.errors(o.cpu(), lse.cpu(), O_ref, L_ref)
