@@ -11,8 +11,12 @@ Timing: W untimed warm-up steps; then K steps, each bracketed by CUDA events
 on the launching stream, with the L2 cache flushed (a 512 MB write) before
 every step, outside the events; barrier + synchronize around the timed
 region; the max over ranks of the summed device time. For N > 1 (launched by
-torchrun) every rank runs its own copy of the workload (independent problems,
-no collective on the data path): weak scaling.
+torchrun; ``--gpus N`` without a torchrun environment starts N ranks itself)
+every rank runs its own copy of the workload (independent problems, no
+collective on the data path): weak scaling. With ``--shard heads`` the ranks
+split the heads of one workload instead (each rank its contiguous range of
+heads, still no collective): strong scaling, value = the workload's FLOPs /
+the slowest rank's time.
 
 The same run also times the backward pass (fa_bwd, two launches) on the
 same workload and reports it under "bwd" (skip with --no-bwd), and a decode
@@ -202,6 +206,32 @@ def dist_setup():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def head_shard(H: int, world: int, rank: int):
+    """[h0, h1): the contiguous range of heads ``rank`` takes when the H heads
+    of one workload are split over ``world`` ranks, as even as possible."""
+    if world < 1 or not 0 <= rank < world:
+        raise ValueError("bad rank / world size")
+    if H < world:
+        raise ValueError(f"cannot split {H} heads over {world} ranks")
+    per, extra = divmod(H, world)
+    h0 = rank * per + min(rank, extra)
+    return h0, h0 + per + (1 if rank < extra else 0)
+
+
+def torchrun_command(n_gpus: int, argv, port: int):
+    """The command that runs this script as ``n_gpus`` ranks on one node (one
+    process per GPU), with the rendezvous on 127.0.0.1."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n_gpus}",
+            "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *argv]
+
+
+def _free_port() -> int:
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
 
 
 def reduce_max(value: float, world: int, device=None) -> float:
@@ -492,6 +522,9 @@ def time_forward(fa, qd, kd, vd, o, lse, scale, flush, stream, steps, warmup, lo
 def run_native(args):
     import torch
     world, rank, local = dist_setup()
+    if args.shard == "heads":
+        # the strong-scaling run times the forward alone
+        args.no_bwd = args.no_comparator = args.no_decode = args.no_per_config = True
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", init_method="env://")
@@ -521,8 +554,12 @@ def run_native(args):
     fa.load_library()
     w = inputs.workload(args.workload)
     q, k, v, scale = inputs.make_inputs(w)
+    if args.shard == "heads":
+        # this rank's contiguous range of the workload's heads
+        h0, h1 = head_shard(w.H, world, rank)
+        q, k, v = (x[:, h0:h1].contiguous() for x in (q, k, v))
     B, H, N, d = q.shape
-    flops = w.flops
+    flops = 4.0 * B * H * N * N * d          # this rank's share (the whole workload unless sharded)
     qd, kd, vd = (x.to(device) for x in (q, k, v))
     o = torch.empty_like(qd)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
@@ -746,22 +783,24 @@ def run_native(args):
         peaks, peak_src = load_peaks()
         avg_ms = sum(step_ms) / len(step_ms)
         achieved = flops / (avg_ms * 1e-3) / 1e12
-        value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+        job_flops = w.flops if args.shard == "heads" else world * flops   # all ranks' work per step
+        value = job_flops * args.steps / (total_ms * 1e-3) / 1e12
         traffic = load_traffic(w.name)
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "scaling": "strong" if args.shard == "heads" else "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded; Q,K ~ N(0,1), V ~ U(-1,1), bf16)",
             "config": {**w.describe(), "l2": "flushed before every step (512 MB write, outside the events)",
-                       "parallelism": f"replicas x{world} (independent problems per rank)"},
+                       "parallelism": (f"heads split over {world} ranks (no collective)" if args.shard == "heads"
+                                       else f"replicas x{world} (independent problems per rank)")},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": UNIT,
                          "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
                          "peak_source": f"{peak_src} dense bf16 burst",
                          "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
                          "kernel": KERNEL_NAME, "flops_per_launch": flops,
                          "algorithmic_bytes_per_launch": B * H * N * (8 * d + 4)},
-            "e2e": {"value": world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+            "e2e": {"value": job_flops * e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / e2e_steps,
                     "api": "fa_fwd_host (C ABI, pinned host buffers; copies pipelined with the kernel)"},
             "gpu_launches": args.steps,
@@ -815,11 +854,23 @@ def main(argv=None):
     ap.add_argument("--no-bwd", action="store_true", help="skip timing the backward pass")
     ap.add_argument("--no-decode", action="store_true", help="skip timing the shared-K/V-head decode shape")
     ap.add_argument("--no-per-config", action="store_true", help="skip timing the other four forward workloads")
+    ap.add_argument("--shard", choices=["none", "heads"], default="none",
+                    help="N > 1: 'none' = every rank runs the whole workload (weak scaling); 'heads' = the ranks "
+                         "split its heads (strong scaling)")
     ap.add_argument("--cfg-cpu-seconds", type=float, default=4.0,
                     help="CPU oracle sample size for each of the other workloads (seconds of work)")
+    raw_argv = list(sys.argv[1:] if argv is None else argv)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
+    env_world = os.environ.get("WORLD_SIZE")
+    if env_world is None and args.gpus > 1:
+        # no torchrun environment: start the N ranks (one per GPU) ourselves
+        return subprocess.call(torchrun_command(args.gpus, raw_argv, _free_port()))
+    if env_world is not None and int(env_world) != args.gpus:
+        ap.error(f"--gpus {args.gpus} does not match WORLD_SIZE={env_world}")
     if args.impl == "reference":
         return run_reference(args)
     return run_native(args)

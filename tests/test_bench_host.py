@@ -126,3 +126,68 @@ def test_committed_traffic_records_match_their_profiles():
         B, H, N, d = 1, 32, 8192, 128
         algorithmic = B * H * N * (8 * d + 4)
         assert algorithmic / 1.5 <= traffic <= 1.5 * algorithmic
+
+
+def test_head_shard_covers_every_head_once():
+    for H in (1, 2, 5, 16, 32, 33):
+        for world in (1, 2, 3, 4, 8):
+            if H < world:
+                with pytest.raises(ValueError):
+                    bench.head_shard(H, world, 0)
+                continue
+            parts = [bench.head_shard(H, world, r) for r in range(world)]
+            assert parts[0][0] == 0 and parts[-1][1] == H
+            assert all(parts[r][1] == parts[r + 1][0] for r in range(world - 1))
+            sizes = [b - a for a, b in parts]
+            assert min(sizes) >= 1 and max(sizes) - min(sizes) <= 1
+
+
+def _shard_rank(rank, world, port, out):
+    """Two gloo ranks split the heads of the 8k prefill workload: each takes its
+    range, the slowest rank's time is the job's, and the job's FLOPs are the
+    workload's, whatever the split."""
+    import torch.distributed as dist
+    from exact_io_aware_34_gb300 import inputs
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    w = inputs.workload("prefill8k_d128_h32")
+    h0, h1 = bench.head_shard(w.H, world, rank)
+    my_flops = 4.0 * w.B * (h1 - h0) * w.N * w.N * w.d
+    total = bench.reduce_max(0.0, world)          # barrier-like exchange
+    t = bench.reduce_max(1.0 + rank, world)       # per-rank seconds; the job takes the slowest
+    import torch
+    flops = torch.tensor([my_flops], dtype=torch.float64)
+    dist.all_reduce(flops)
+    out[rank] = (h0, h1, t, float(flops.item()), total)
+    dist.destroy_process_group()
+
+
+def test_head_shard_two_gloo_ranks():
+    from exact_io_aware_34_gb300 import inputs
+    world = 2
+    with mp.Manager() as man:
+        out = man.dict()
+        mp.spawn(_shard_rank, args=(world, _free_port(), out), nprocs=world, join=True)
+        res = dict(out)
+    w = inputs.workload("prefill8k_d128_h32")
+    assert res[0][:2] == (0, 16) and res[1][:2] == (16, 32)
+    assert res[0][2] == res[1][2] == 2.0
+    assert res[0][3] == w.flops          # the ranks' shares add up to the whole workload
+
+
+def test_gpus_flag_relaunches_under_torchrun(monkeypatch):
+    calls = []
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    monkeypatch.setattr(bench.subprocess, "call", lambda cmd: calls.append(cmd) or 0)
+    assert bench.main(["--gpus", "4", "--steps", "3", "--warmup", "3", "--shard", "heads"]) == 0
+    cmd = calls[0]
+    assert cmd[1:4] == ["-m", "torch.distributed.run", "--nnodes=1"] and "--nproc-per-node=4" in cmd
+    assert cmd[cmd.index("--master-addr") + 1] == "127.0.0.1"
+    assert cmd[cmd.index(os.path.abspath(bench.__file__)) + 1:] == ["--gpus", "4", "--steps", "3", "--warmup", "3", "--shard", "heads"]
+
+
+def test_gpus_flag_must_match_world_size(monkeypatch):
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    with pytest.raises(SystemExit):
+        bench.main(["--gpus", "4"])
