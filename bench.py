@@ -51,7 +51,6 @@ if ROOT not in sys.path:
 METRIC = "attention fwd TFLOP/s (4·B·H·N²·d) and % of GB300 dense BF16 peak, 1 GPU"
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "prefill8k_d128_h32"
-KERNEL_NAME = "fa_fwd_kernel<128>"
 # Sources that determine each kernel's machine code: a committed DRAM-traffic
 # figure is used only while these are unchanged since its capture.
 KERNEL_SOURCES = ["exact_io_aware_34_gb300/csrc/fa_fwd_kernel.cuh", "exact_io_aware_34_gb300/csrc/sm103a_ptx.cuh"]
@@ -798,7 +797,7 @@ def run_native(args):
                          "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
                          "peak_source": f"{peak_src} dense bf16 burst",
                          "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
-                         "kernel": KERNEL_NAME, "flops_per_launch": flops,
+                         "kernel": f"fa_fwd_kernel<{d}>", "flops_per_launch": flops,
                          "algorithmic_bytes_per_launch": B * H * N * (8 * d + 4)},
             "e2e": {"value": job_flops * e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / e2e_steps,

@@ -259,7 +259,8 @@ __global__ void __launch_bounds__(DecCfg<HD>::kThreads, DecCfg<HD>::kCtasPerSm)
     const uint32_t tO = tmem_base + lane_addr + C::kColO;
     const float sl2 = p.scale_log2;
     float m_use = 0.f;
-    float l = 0.f;
+    float l = 0.f;          // running sum of exp, relative to m_use (for LSE)
+    float lo = 0.f;         // the same with each block's largest term as P V sees it (for O)
     bool ok = true;
     for (int jj = 0; jj < n; ++jj) {
       ok = wait_warp_or_abort(ptx::smem_u32(&bar_s_full), jj & 1, abort_ptr, p.timeout_ns, kRoleDecSoftmax);
@@ -334,7 +335,14 @@ __global__ void __launch_bounds__(DecCfg<HD>::kThreads, DecCfg<HD>::kCtasPerSm)
         ptx::f2_unpack(ptx::f2_add(acc[2], acc[3]), b0, b1);
         sum = (a0 + a1) + (b0 + b1);
       }
+      // The P V product sees every probability rounded to bf16. The largest
+      // one of the block (the score equal to mt, recomputed here exactly as
+      // the loop above computes it) enters the normaliser of O the same way,
+      // so that a row dominated by one key weights it exactly 1; l itself,
+      // which LSE needs, stays the sum of the unrounded terms.
+      const float pmax = ptx::ex2_approx(fmaf(mt, sl2, neg_m));
       l = l * alpha + sum;
+      lo = lo * alpha + (sum + (ptx::round_bf16(pmax) - pmax));
       ptx::tmem_st32(tS, pk[0]);
       ptx::tmem_st32(tS + 32, pk[1]);
       if (rescale_o) {
@@ -360,7 +368,7 @@ __global__ void __launch_bounds__(DecCfg<HD>::kThreads, DecCfg<HD>::kCtasPerSm)
       const bool in_range = row < rows;
       const int hq = row / p.box_q;
       const size_t grow = (static_cast<size_t>(bh_q0) + hq) * p.N_q + q0 + (row - hq * p.box_q);
-      const float inv_l = 1.f / l;
+      const float inv_l = 1.f / lo;
       const float lse = (m_use * sl2 + __log2f(l)) * 0.69314718055994530942f;
       const size_t n_rows = static_cast<size_t>(gridDim.z) * p.H * p.N_q;
 #pragma unroll

@@ -339,7 +339,8 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
     const uint32_t tO = tmem_base + lane_addr + C::kColO + HD * t;
     const float sl2 = p.scale_log2;
     float m_use = 0.f;      // raw-score maximum the exponentials are taken against
-    float l = 0.f;          // running sum of exp, relative to m_use
+    float l = 0.f;          // running sum of exp, relative to m_use (for LSE)
+    float lo = 0.f;         // the same with each block's largest term as P V sees it (for O)
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       // V_j and K_{j+1} must have landed before this block's hand-off (see
@@ -439,7 +440,14 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
         ptx::f2_unpack(ptx::f2_add(acc[2], acc[3]), b0, b1);
         sum = (a0 + a1) + (b0 + b1);
       }
+      // The P V product sees every probability rounded to bf16. The largest
+      // one of the block (the score equal to mt, recomputed here exactly as
+      // the loop above computes it) enters the normaliser of O the same way,
+      // so that a row dominated by one key weights it exactly 1; l itself,
+      // which LSE needs, stays the sum of the unrounded terms.
+      const float pmax = ptx::ex2_approx(fmaf(mt, sl2, neg_m));
       l = l * alpha + sum;
+      lo = lo * alpha + (sum + (ptx::round_bf16(pmax) - pmax));
       ptx::tmem_st32(tS, pk[0]);
       ptx::tmem_st32(tS + 32, pk[1]);
       if (rescale_o) {
@@ -463,7 +471,7 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
       ptx::tc_fence_after();
       const int grow = q_row0 + t * C::kBM + row;
       const bool in_range = grow < p.N;
-      const float inv_l = 1.f / l;
+      const float inv_l = 1.f / lo;
       __nv_bfloat16* orow = p.O + (static_cast<size_t>(bh) * p.N + grow) * HD;
 #pragma unroll
       for (int c = 0; c < HD / 32; ++c) {

@@ -416,5 +416,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// x rounded to bf16 by the same conversion pack_bf16x2 makes, as a float.
+__device__ __forceinline__ float round_bf16(float x) { return __uint_as_float(pack_bf16x2(x, 0.f) << 16); }
+
 }  // namespace ptx
 }  // namespace fa
