@@ -72,6 +72,18 @@ bool make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
   return r == CUDA_SUCCESS;
 }
 
+// SM count of a device, read once per device.
+int sm_count(int dev) {
+  static std::once_flag once[64];
+  static int count[64];
+  std::call_once(once[dev], [dev] {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    count[dev] = n;
+  });
+  return count[dev];
+}
+
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   auto x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
   return x < y + nb && y < x + na;
@@ -88,11 +100,20 @@ fa_status_t launch(const void* Q, const void* K, const void* V, void* O, float* 
   static std::once_flag attr_once[64];
   static cudaError_t attr_err[64];
   if (dev < 0 || dev >= 64) return FA_ERR_UNSUPPORTED;
+  static bool regs_ok[64];
   std::call_once(attr_once[dev], [&] {
     attr_err[dev] = cudaFuncSetAttribute(fa::fa_fwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
+    // The warpgroups' register split draws on the registers the block is
+    // launched with; a split larger than that would never complete, so the
+    // kernel is not launched unless the built register count covers it.
+    cudaFuncAttributes fattr;
+    if (attr_err[dev] == cudaSuccess) attr_err[dev] = cudaFuncGetAttributes(&fattr, fa::fa_fwd_kernel<HD>);
+    regs_ok[dev] = attr_err[dev] == cudaSuccess &&
+                   8 * C::kRegsSoftmax + 4 * C::kRegsControl <= 12 * fattr.numRegs;
   });
   if (attr_err[dev] != cudaSuccess) return cuda_fail(attr_err[dev]);
+  if (!regs_ok[dev]) return FA_ERR_UNSUPPORTED;
 
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, Q, B * H, N, HD) || !make_map(&mk, K, B * H_kv, N_kv, HD) ||
@@ -107,13 +128,17 @@ fa_status_t launch(const void* Q, const void* K, const void* V, void* O, float* 
   p.H = H;
   p.H_kv = H_kv;
   p.n_kv_blocks = (N_kv + C::kBN - 1) / C::kBN;
+  p.q_blocks = (N + C::kQTiles * C::kBM - 1) / (C::kQTiles * C::kBM);
+  p.num_units = B * H * p.q_blocks;   // < 2^31 / 256: B*H*N < 2^31
   // scale < 0: the tensor core forms -S and the kernel runs with |scale|.
   p.scale_log2 = static_cast<float>(std::fabs(static_cast<double>(scale)) * 1.4426950408889634074);
   p.idesc_qk = C::kIdescQK | (scale < 0.f ? fa::ptx::kIdescNegateA : 0u);
   p.timeout_ns = timeout_ns;
   p.drop_load = drop_load;
 
-  dim3 grid((N + C::kQTiles * C::kBM - 1) / (C::kQTiles * C::kBM), H, B);
+  // Persistent grid: one CTA per SM (the kernel's shared memory and tensor
+  // memory allow no second), each walking units blockIdx.x + k * gridDim.x.
+  const unsigned grid = static_cast<unsigned>(std::min(p.num_units, sm_count(dev)));
   fa::fa_fwd_kernel<HD><<<grid, C::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);

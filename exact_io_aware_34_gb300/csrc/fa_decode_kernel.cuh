@@ -266,33 +266,42 @@ __global__ void __launch_bounds__(DecCfg<HD>::kThreads, DecCfg<HD>::kCtasPerSm)
       ok = wait_warp_or_abort(ptx::smem_u32(&bar_s_full), jj & 1, abort_ptr, p.timeout_ns, kRoleDecSoftmax);
       if (!ok) break;
       ptx::tc_fence_after();
+      // The loads also reduce each 32-column piece to its maximum, which is
+      // the row maximum of a full block; the ragged last block masks the
+      // columns past N_kv (scores of zero-filled keys) and takes its own.
       uint32_t s[4][32];
+      float mr[4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + 32 * c, s[c]);
+      for (int c = 0; c < 4; ++c) ptx::tmem_ld32_max(tS + 32 * c, s[c], mr[c]);
       ptx::tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) ptx::reg_fence32(s[c]);
+      for (int c = 0; c < 4; ++c) {
+        ptx::reg_fence32(s[c]);
+        ptx::reg_fence1(mr[c]);
+      }
 
       const int valid = p.N_kv - (j0 + jj) * C::kBN;   // keys of this block that exist
       const bool ragged = valid < C::kBN;
-      if (ragged) {
+      float mt;
+      if (!ragged) {
+        mt = ptx::max3(mr[0], mr[1], fmaxf(mr[2], mr[3]));
+      } else {
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int i = 0; i < 32; ++i)
             if (32 * c + i >= valid) s[c][i] = __float_as_uint(-INFINITY);
-      }
-      float mc[8];
+        float mc[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int c = k >> 1, bb = (k & 1) * 16;
-        mc[k] = fmaxf(__uint_as_float(s[c][bb]), __uint_as_float(s[c][bb + 1]));
+        for (int k = 0; k < 8; ++k) {
+          const int c = k >> 1, bb = (k & 1) * 16;
+          mc[k] = fmaxf(__uint_as_float(s[c][bb]), __uint_as_float(s[c][bb + 1]));
 #pragma unroll
-        for (int i = 2; i < 16; i += 2)
-          mc[k] = ptx::max3(mc[k], __uint_as_float(s[c][bb + i]), __uint_as_float(s[c][bb + i + 1]));
+          for (int i = 2; i < 16; i += 2)
+            mc[k] = ptx::max3(mc[k], __uint_as_float(s[c][bb + i]), __uint_as_float(s[c][bb + i + 1]));
+        }
+        mt = ptx::max3(ptx::max3(mc[0], mc[1], mc[2]), ptx::max3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
       }
-      const float mt = ptx::max3(ptx::max3(mc[0], mc[1], mc[2]), ptx::max3(mc[3], mc[4], mc[5]),
-                                 fmaxf(mc[6], mc[7]));
       float alpha = 1.f;
       bool rescale_o = false;
       if (jj == 0) {
@@ -327,6 +336,9 @@ __global__ void __launch_bounds__(DecCfg<HD>::kThreads, DecCfg<HD>::kCtasPerSm)
           acc[(i >> 1) & 3] = ptx::f2_add(acc[(i >> 1) & 3], ptx::f2_pack(p0, p1));
           pk[c >> 1][(c & 1) * 16 + (i >> 1)] = ptx::pack_bf16x2(p0, p1);
         }
+        // The first 64 probabilities are packed: store them now (over scores
+        // already in registers) and free their registers.
+        if (c == 1) ptx::tmem_st32(tS, pk[0]);
       }
       float sum;
       {
@@ -343,7 +355,6 @@ __global__ void __launch_bounds__(DecCfg<HD>::kThreads, DecCfg<HD>::kCtasPerSm)
       const float pmax = ptx::ex2_approx(fmaf(mt, sl2, neg_m));
       l = l * alpha + sum;
       lo = lo * alpha + (sum + (ptx::round_bf16(pmax) - pmax));
-      ptx::tmem_st32(tS, pk[0]);
       ptx::tmem_st32(tS + 32, pk[1]);
       if (rescale_o) {
 #pragma unroll

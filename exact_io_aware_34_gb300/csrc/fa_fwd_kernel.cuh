@@ -1,7 +1,8 @@
 // Fused exact-attention forward kernel for sm_103a (tcgen05 + TMEM + TMA).
 //
-// One CTA owns 2 query tiles of 128 rows (256 query rows) of one (b, h) and
-// streams every 128-row key/value block of that head past them:
+// A unit of work is 2 query tiles of 128 rows (256 query rows) of one (b, h);
+// the CTA that owns it streams every 128-row key/value block of that head
+// past them:
 //   "Flash Attention (FA1)", "Tiling in FlashAttention": Q in Br x d blocks,
 //   K and V in Bc x d blocks, Tc = ceil(N / Bc); here Br = Bc = 128 (the
 //   tcgen05 M and the key-block width). The CTA runs the query-outer order
@@ -30,12 +31,25 @@
 // stay below 2^kRescaleLog2, far inside bf16/fp32 range. This skips most of
 // the O rescales (a TMEM read-modify-write of 128 x d floats).
 //
-// Warp roles (10 warps):
-//   warps 0-3  softmax + epilogue for query tile 0 (one thread per row)
-//   warps 4-7  softmax + epilogue for query tile 1
-//   warp 8     TMA producer (one thread)
-//   warp 9     TMEM allocator and MMA issuer (the whole warp, converged; one
-//              elected lane issues each tcgen05 instruction)
+// Persistent grid: one CTA per SM (shared and tensor memory allow no
+// second) walks units blockIdx.x, blockIdx.x + gridDim.x, ... in (b, h,
+// query block) order, so the CTAs in flight share few heads' K/V in L2. The
+// ring position and the barrier phases run on across units: the next unit's
+// Q is loaded as soon as the last Q K^T products of the current one have
+// completed, and its first Q K^T products are issued right after the current
+// unit's last P V, so they overlap that unit's epilogue.
+//
+// Warp roles (12 warps, 3 warpgroups):
+//   warps 0-3   softmax + epilogue for query tile 0 (one thread per row)
+//   warps 4-7   softmax + epilogue for query tile 1
+//   warp 8      TMA producer (one thread)
+//   warp 9      TMEM allocator and MMA issuer (the whole warp, converged; one
+//               elected lane issues each tcgen05 instruction)
+//   warps 10-11 idle (they complete the third warpgroup)
+// With 12 warps a launch gets 168 registers per thread (3 warps per SM
+// sub-partition); setmaxnreg then moves registers from the control
+// warpgroup (down to 72) to the softmax warpgroups (up to 216), which hold a
+// 128-score row plus its packed probabilities without spilling.
 // TMEM (512 columns x 128 lanes x 32 bit): S_t at column 128*t (P_t, packed
 // bf16, overwrites the first 64 of those columns), O_t at 256 + d*t.
 // Shared memory: Q tiles (2 x 128 x d bf16) + a ring of K/V tiles
@@ -71,7 +85,15 @@ struct FwdCfg {
   static constexpr int kSmemQ = kQTiles * kTileBytes;
   static constexpr int kSmemKV = kStages * kTileBytes;
   static constexpr int kSmemBytes = kSmemQ + kSmemKV + 1024;  // + alignment slack
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = 384;          // 12 warps: 3 warpgroups
+  // Registers per thread after the split: the two softmax warpgroups raise
+  // theirs, the control warpgroup (producer, MMA issuer, two idle warps)
+  // lowers its own. The launch holds 12 warps x 32 x kRegsLaunch registers;
+  // the split must not need more (the host checks the built kernel's count).
+  static constexpr int kRegsLaunch = 168;
+  static constexpr int kRegsSoftmax = 216;
+  static constexpr int kRegsControl = 72;
+  static_assert(8 * kRegsSoftmax + 4 * kRegsControl <= 12 * kRegsLaunch, "register split exceeds the launch");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0;         // + 128 * t
   static constexpr uint32_t kColO = 256;       // + HD * t
@@ -87,6 +109,8 @@ struct FwdParams {
   int H;                       // query heads
   int H_kv;                    // K/V heads; query head h reads K/V head h / (H / H_kv)
   int n_kv_blocks;
+  int q_blocks;                // 256-row query blocks per head
+  int num_units;               // B * H * q_blocks: the (b, h, query block) units the CTAs walk
   float scale_log2;            // |scale| * log2(e)
   uint32_t idesc_qk;           // instruction descriptor of S = Q K^T (A negated when scale < 0)
   unsigned long long timeout_ns;
@@ -165,6 +189,7 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
   using C = FwdCfg<HD>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_q_full;
+  __shared__ __align__(8) uint64_t bar_q_empty;
   __shared__ __align__(8) uint64_t bar_kv_full[C::kStages];
   __shared__ __align__(8) uint64_t bar_kv_empty[C::kStages];
   __shared__ __align__(8) uint64_t bar_s_full[2];
@@ -176,10 +201,15 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.z * p.H + blockIdx.y;
-  const int bh_kv = blockIdx.z * p.H_kv + blockIdx.y / (p.H / p.H_kv);
-  const int q_row0 = blockIdx.x * (C::kQTiles * C::kBM);
   const int n_kv = p.n_kv_blocks;
+  // Unit u is query block u % q_blocks of head u / q_blocks; this CTA takes
+  // units blockIdx.x, blockIdx.x + gridDim.x, ...
+  auto unit_head = [&](int u) { return u / p.q_blocks; };
+  auto unit_row0 = [&](int u) { return (u - (u / p.q_blocks) * p.q_blocks) * (C::kQTiles * C::kBM); };
+  auto kv_head = [&](int bh) {
+    const int b = bh / p.H;
+    return b * p.H_kv + (bh - b * p.H) / (p.H / p.H_kv);
+  };
 
   // 1024-byte aligned base: the 128-byte swizzle pattern is a function of
   // the shared-memory address bits [4, 10).
@@ -189,6 +219,7 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(ptx::smem_u32(&bar_q_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&bar_q_empty), 1);
     for (int s = 0; s < C::kStages; ++s) {
       ptx::mbar_init(ptx::smem_u32(&bar_kv_full[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&bar_kv_empty[s]), 1);
@@ -217,42 +248,55 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
   const uint32_t tmem_base = tmem_base_slot;
   volatile int* abort_ptr = &abort_flag;
 
+  if (warp >= 8) ptx::setmaxnreg_dec<C::kRegsControl>();
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t pol_q = ptx::policy_evict_first();
       const uint64_t pol_kv = ptx::policy_evict_last();
       const uint32_t q_full = ptx::smem_u32(&bar_q_full);
-      ptx::mbar_arrive_expect_tx(q_full, C::kQTiles * C::kTileBytes);
-      for (int t = 0; t < C::kQTiles; ++t)
-        for (int c = 0; c < C::kChunks; ++c)
-          ptx::tma_load_3d(sQ + t * C::kTileBytes + c * C::kChunkBytes, &tmQ, q_full, c * 64,
-                           q_row0 + t * C::kBM, bh, pol_q);
-      int issued = 0;
+      int issued = 0;       // K/V loads issued by this CTA (the ring position runs on across units)
+      int q_issued = 0;     // Q loads issued (one per unit)
       bool ok = true;
-      for (int j = 0; j < n_kv && ok; ++j) {
-        for (int kv = 0; kv < 2; ++kv) {
-          const int it = 2 * j + kv;
-          const int slot = it % C::kStages;
-          const uint32_t phase = (it / C::kStages) & 1;
-          if (!wait_or_abort(ptx::smem_u32(&bar_kv_empty[slot]), phase ^ 1u, abort_ptr, p.timeout_ns,
-                             kRoleProducer)) {
-            ok = false;
-            break;
-          }
-          issued = it + 1;
-          if (it == p.drop_load) continue;   // test hook: this tile never arrives
-          const uint32_t full = ptx::smem_u32(&bar_kv_full[slot]);
-          ptx::mbar_arrive_expect_tx(full, C::kTileBytes);
-          const void* map = kv ? static_cast<const void*>(&tmV) : static_cast<const void*>(&tmK);
+      int uc = 0;
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+        const int bh = unit_head(u), bh_kv = kv_head(bh), q_row0 = unit_row0(u);
+        // The previous unit's Q tiles are free once its last Q K^T products completed.
+        if (uc > 0 && !wait_or_abort(ptx::smem_u32(&bar_q_empty), (uc - 1) & 1, abort_ptr, p.timeout_ns,
+                                     kRoleProducer)) {
+          ok = false;
+          break;
+        }
+        ptx::mbar_arrive_expect_tx(q_full, C::kQTiles * C::kTileBytes);
+        for (int t = 0; t < C::kQTiles; ++t)
           for (int c = 0; c < C::kChunks; ++c)
-            ptx::tma_load_3d(sKV + slot * C::kTileBytes + c * C::kChunkBytes, map, full, c * 64,
-                             j * C::kBN, bh_kv, pol_kv);
+            ptx::tma_load_3d(sQ + t * C::kTileBytes + c * C::kChunkBytes, &tmQ, q_full, c * 64,
+                             q_row0 + t * C::kBM, bh, pol_q);
+        q_issued = uc + 1;
+        for (int j = 0; j < n_kv && ok; ++j) {
+          for (int kv = 0; kv < 2; ++kv) {
+            const int it = 2 * n_kv * uc + 2 * j + kv;
+            const int slot = it % C::kStages;
+            const uint32_t phase = (it / C::kStages) & 1;
+            if (!wait_or_abort(ptx::smem_u32(&bar_kv_empty[slot]), phase ^ 1u, abort_ptr, p.timeout_ns,
+                               kRoleProducer)) {
+              ok = false;
+              break;
+            }
+            issued = it + 1;
+            if (it == p.drop_load) continue;   // test hook: this tile never arrives
+            const uint32_t full = ptx::smem_u32(&bar_kv_full[slot]);
+            ptx::mbar_arrive_expect_tx(full, C::kTileBytes);
+            const void* map = kv ? static_cast<const void*>(&tmV) : static_cast<const void*>(&tmK);
+            for (int c = 0; c < C::kChunks; ++c)
+              ptx::tma_load_3d(sKV + slot * C::kTileBytes + c * C::kChunkBytes, map, full, c * 64,
+                               j * C::kBN, bh_kv, pol_kv);
+          }
         }
       }
       if (!ok || *abort_ptr) {
         // Let every copy this thread started land before the CTA exits.
-        drain_wait(q_full, 0, p.timeout_ns);
+        if (q_issued > 0) drain_wait(q_full, (q_issued - 1) & 1, p.timeout_ns);
         const int first = issued > C::kStages ? issued - C::kStages : 0;
         for (int it = first; it < issued; ++it) {
           if (it == p.drop_load) continue;
@@ -267,22 +311,19 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
     // elected lane issues every tcgen05 instruction. A lone diverged lane
     // issues far more slowly while the softmax warps of its sub-partition
     // compete for issue slots.
-    bool ok = wait_warp_or_abort(ptx::smem_u32(&bar_q_full), 0, abort_ptr, p.timeout_ns, kRoleMma);
-    ptx::tc_fence_after();
-    // P V for query tile t and key block jj (P_t sits in the S_t columns).
-    auto issue_pv = [&](int t, int jj) {
-      const int it = 2 * jj + 1;
+    // P V for query tile t from the V tile loaded as the it-th K/V load (P_t
+    // sits in the S_t columns); the first product of a unit overwrites O_t.
+    auto issue_pv = [&](int t, int it, bool accumulate) {
       const uint32_t v_tile = sKV + (it % C::kStages) * C::kTileBytes;
       const uint32_t d_tmem = tmem_base + C::kColO + HD * t;
       const uint32_t a_tmem = tmem_base + C::kColS + 128 * t;
       static_assert(C::kBN == 128, "one burst of eight K = 16 products");
       const uint64_t b_desc = ptx::desc_mnmajor_sw128(v_tile, C::kChunkBytes);
       ptx::mma_ts_k128_warp<32>(d_tmem, a_tmem, ptx::desc_lo(b_desc), ptx::desc_hi(b_desc), C::kIdescPV,
-                                jj > 0 ? 1u : 0u);
+                                accumulate ? 1u : 0u);
     };
-    // S_t = Q_t K_j^T.
-    auto issue_qk = [&](int t, int j) {
-      const int it = 2 * j;
+    // S_t = Q_t K^T with the K tile of the it-th K/V load.
+    auto issue_qk = [&](int t, int it) {
       const uint32_t k_tile = sKV + (it % C::kStages) * C::kTileBytes;
       const uint32_t q_tile = sQ + t * C::kTileBytes;
       const uint32_t d_tmem = tmem_base + C::kColS + 128 * t;
@@ -292,36 +333,50 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
       else
         ptx::mma_ss_k64_warp(d_tmem, ptx::desc_lo(a_desc), ptx::desc_lo(b_desc), ptx::desc_hi(a_desc), p.idesc_qk, 0u);
     };
-    // K_0 is waited for here; every later K_{j+1} and V_j is waited for by
-    // the softmax warps before their hand-off for block j (p_full), so the
-    // p_full waits below imply those tiles have landed. An mbarrier wait in
-    // this warp stalls the queued tensor-core work, so it does as few as it
-    // can.
-    if (ok) ok = wait_warp_or_abort(ptx::smem_u32(&bar_kv_full[0]), 0, abort_ptr, p.timeout_ns, kRoleMma);
-    for (int j = 0; j < n_kv && ok; ++j) {
-      const int itK = 2 * j;
-      ptx::tc_fence_after();
-      for (int t = 0; t < 2 && ok; ++t) {
-        if (j > 0) {
-          ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_full[t]), (j - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
-          if (!ok) break;
-          ptx::tc_fence_after();
-          issue_pv(t, j - 1);
-          if (t == 1) ptx::mma_commit_warp(ptx::smem_u32(&bar_kv_empty[(2 * (j - 1) + 1) % C::kStages]));
+    // Per unit: Q and K_0 are waited for here; every later K_{j+1} and V_j
+    // is waited for by the softmax warps before their hand-off for block j
+    // (p_full), so the p_full waits below imply those tiles have landed. An
+    // mbarrier wait in this warp stalls the queued tensor-core work, so it
+    // does as few as it can. g counts the key blocks of all units so far
+    // (the phase of s_full / p_full).
+    bool ok = true;
+    int g = 0, uc = 0;
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+      const int it0 = 2 * n_kv * uc;
+      ok = wait_warp_or_abort(ptx::smem_u32(&bar_q_full), uc & 1, abort_ptr, p.timeout_ns, kRoleMma);
+      if (ok)
+        ok = wait_warp_or_abort(ptx::smem_u32(&bar_kv_full[it0 % C::kStages]), (it0 / C::kStages) & 1, abort_ptr,
+                                p.timeout_ns, kRoleMma);
+      for (int j = 0; j < n_kv && ok; ++j, ++g) {
+        const int itK = it0 + 2 * j;
+        ptx::tc_fence_after();
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j > 0) {
+            ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_full[t]), (g - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            issue_pv(t, itK - 1, j > 1);
+            if (t == 1) ptx::mma_commit_warp(ptx::smem_u32(&bar_kv_empty[(itK - 1) % C::kStages]));
+          }
+          issue_qk(t, itK);
+          ptx::mma_commit_warp(ptx::smem_u32(&bar_s_full[t]));
         }
-        issue_qk(t, j);
-        ptx::mma_commit_warp(ptx::smem_u32(&bar_s_full[t]));
+        if (ok) {
+          ptx::mma_commit_warp(ptx::smem_u32(&bar_kv_empty[itK % C::kStages]));
+          // The unit's last Q K^T products are issued: Q is free when they complete.
+          if (j == n_kv - 1) ptx::mma_commit_warp(ptx::smem_u32(&bar_q_empty));
+        }
       }
-      if (ok) ptx::mma_commit_warp(ptx::smem_u32(&bar_kv_empty[itK % C::kStages]));
-    }
-    // The last key block's P V.
-    for (int t = 0; t < 2 && ok; ++t) {
-      ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_full[t]), (n_kv - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
-      if (!ok) break;
-      ptx::tc_fence_after();
-      issue_pv(t, n_kv - 1);
-      ptx::mma_commit_warp(ptx::smem_u32(&bar_o_full[t]));
-      if (t == 1) ptx::mma_commit_warp(ptx::smem_u32(&bar_kv_empty[(2 * (n_kv - 1) + 1) % C::kStages]));
+      // The last key block's P V.
+      const int itV = it0 + 2 * n_kv - 1;
+      for (int t = 0; t < 2 && ok; ++t) {
+        ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_full[t]), (g - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        issue_pv(t, itV, n_kv > 1);
+        ptx::mma_commit_warp(ptx::smem_u32(&bar_o_full[t]));
+        if (t == 1) ptx::mma_commit_warp(ptx::smem_u32(&bar_kv_empty[itV % C::kStages]));
+      }
     }
     if (!ok) {
       // Wait for every MMA already issued before TMEM is freed.
@@ -329,8 +384,9 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
       drain_wait(ptx::smem_u32(&bar_drain), 0, p.timeout_ns);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ softmax + epilogue
+    ptx::setmaxnreg_inc<C::kRegsSoftmax>();
     const int t = warp >> 2;                 // query tile
     const int quarter = warp & 3;            // TMEM lane quarter
     const int row = quarter * 32 + lane;     // row within the tile
@@ -338,15 +394,18 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
     const uint32_t tS = tmem_base + lane_addr + C::kColS + 128 * t;
     const uint32_t tO = tmem_base + lane_addr + C::kColO + HD * t;
     const float sl2 = p.scale_log2;
+    bool ok = true;
+    int g = 0, uc = 0;      // key blocks and units so far (barrier phases)
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+    const int it0 = 2 * n_kv * uc;
     float m_use = 0.f;      // raw-score maximum the exponentials are taken against
     float l = 0.f;          // running sum of exp, relative to m_use (for LSE)
     float lo = 0.f;         // the same with each block's largest term as P V sees it (for O)
-    bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
+    for (int j = 0; j < n_kv; ++j, ++g) {
       // V_j and K_{j+1} must have landed before this block's hand-off (see
       // the MMA issuer); waiting here costs nothing, S_t(j) comes later.
       {
-        const int itV = 2 * j + 1;
+        const int itV = it0 + 2 * j + 1;
         ok = wait_warp_or_abort(ptx::smem_u32(&bar_kv_full[itV % C::kStages]), (itV / C::kStages) & 1, abort_ptr,
                                 p.timeout_ns, kRoleSoftmax);
         if (ok && j + 1 < n_kv)
@@ -354,7 +413,7 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
                                   abort_ptr, p.timeout_ns, kRoleSoftmax);
         if (!ok) break;
       }
-      ok = wait_warp_or_abort(ptx::smem_u32(&bar_s_full[t]), j & 1, abort_ptr, p.timeout_ns, kRoleSoftmax);
+      ok = wait_warp_or_abort(ptx::smem_u32(&bar_s_full[t]), g & 1, abort_ptr, p.timeout_ns, kRoleSoftmax);
       if (!ok) break;
       ptx::tc_fence_after();
       // The loads also reduce each 32-column piece to its maximum, which is
@@ -466,10 +525,11 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
       ptx::tc_fence_before();
       ptx::mbar_arrive(ptx::smem_u32(&bar_p_full[t]));
     }
-    if (ok) ok = wait_warp_or_abort(ptx::smem_u32(&bar_o_full[t]), 0, abort_ptr, p.timeout_ns, kRoleSoftmax);
+    if (ok) ok = wait_warp_or_abort(ptx::smem_u32(&bar_o_full[t]), uc & 1, abort_ptr, p.timeout_ns, kRoleSoftmax);
     if (ok) {
       ptx::tc_fence_after();
-      const int grow = q_row0 + t * C::kBM + row;
+      const int bh = unit_head(u);
+      const int grow = unit_row0(u) + t * C::kBM + row;
       const bool in_range = grow < p.N;
       const float inv_l = 1.f / lo;
       __nv_bfloat16* orow = p.O + (static_cast<size_t>(bh) * p.N + grow) * HD;
@@ -495,6 +555,7 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
         p.LSE[static_cast<size_t>(bh) * p.N + grow] = (m_use * sl2 + __log2f(l)) * 0.69314718055994530942f;
       }
     }
+    }   // units
   }
 
   ptx::tc_fence_before();

@@ -111,7 +111,11 @@ def test_committed_traffic_records_match_their_profiles():
     with open(bench.TRAFFIC_FILE) as f:
         rec = json.load(f)
     summaries = {
-        "prefill8k_d128_h32": "fa_fwd_kernel_prefill8k_d128.md",
+        "prefill8k_d128_h32": "dram_traffic_all_workloads.md",
+        "n256_d64": "dram_traffic_all_workloads.md",
+        "n1024_d64_b4h16": "dram_traffic_all_workloads.md",
+        "n4096_d128_b2h16": "dram_traffic_all_workloads.md",
+        "long32k_d128_h16_spiky": "dram_traffic_all_workloads.md",
         "prefill8k_d128_h32:bwd": "fa_bwd_kernels_prefill8k_d128.md",
         "decode32k_gqa8_b4": "fa_decode_kernel_decode32k_gqa8.md",
     }
@@ -121,11 +125,14 @@ def test_committed_traffic_records_match_their_profiles():
         assert e["dram_bytes_read"] + e["dram_bytes_write"] == e["dram_bytes_per_launch"], key
         with open(os.path.join(os.path.dirname(bench.TRAFFIC_FILE), md)) as f:
             assert e["kernel_source_hash"] in f.read(), (key, md)
-    traffic = bench.load_traffic("prefill8k_d128_h32")
-    if traffic is not None:
-        B, H, N, d = 1, 32, 8192, 128
-        algorithmic = B * H * N * (8 * d + 4)
-        assert algorithmic / 1.5 <= traffic <= 1.5 * algorithmic
+    from exact_io_aware_34_gb300 import inputs
+    for w in inputs.WORKLOADS:
+        if w.name not in rec or bench.load_traffic(w.name) is None:
+            continue
+        reads = rec[w.name]["dram_bytes_read"]
+        inputs_bytes = 3 * w.B * w.H * w.N * w.d * 2          # Q, K, V once
+        assert inputs_bytes / 1.05 <= reads <= 1.05 * inputs_bytes + (1 << 20), w.name
+        assert rec[w.name]["dram_bytes_per_launch"] <= 1.5 * w.B * w.H * w.N * (8 * w.d + 4) + (1 << 20), w.name
 
 
 def test_head_shard_covers_every_head_once():
