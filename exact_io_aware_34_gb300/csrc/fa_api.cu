@@ -138,8 +138,42 @@ fa_status_t launch(const void* Q, const void* K, const void* V, void* O, float* 
 
   // Persistent grid: one CTA per SM (the kernel's shared memory and tensor
   // memory allow no second), each walking units blockIdx.x + k * gridDim.x.
-  const unsigned grid = static_cast<unsigned>(std::min(p.num_units, sm_count(dev)));
-  fa::fa_fwd_kernel<HD><<<grid, C::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, p);
+  // When the units left after the whole rounds would occupy at most half of
+  // an even grid, the grid is launched as clusters of two CTAs and each pair
+  // shares one of those units, half of its key blocks each: the last round
+  // then takes about half as long.
+  const int sms = sm_count(dev);
+  int grid = std::min(p.num_units, sms);
+  p.num_whole = p.num_units;
+  p.split_tail = 0;
+  const int even = sms & ~1;
+  if (p.n_kv_blocks >= 4 && even >= 2) {   // at least two key blocks for each half
+    const int whole = p.num_units / even;
+    const int tail = p.num_units - whole * even;
+    if (tail > 0 && 2 * tail <= even) {
+      p.split_tail = 1;
+      p.num_whole = whole * even;
+      grid = even;
+    }
+  }
+  if (p.split_tail) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, fa::fa_fwd_kernel<HD>, mq, mk, mv, p);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return FA_OK;
+  }
+  fa::fa_fwd_kernel<HD><<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   return FA_OK;

@@ -39,6 +39,19 @@
 // completed, and its first Q K^T products are issued right after the current
 // unit's last P V, so they overlap that unit's epilogue.
 //
+// Split last round. All units cost the same, so a grid of G CTAs takes
+// ceil(units / G) rounds. When the units left after the whole rounds would
+// fill at most half of an even grid, the host launches clusters of two CTAs
+// and each pair shares one of those units: rank r runs the r-th half of its
+// key blocks and keeps an unmerged partial result (O relative to its own
+// running maximum, with m, l and l'). Then rank r finalises query tile r:
+// the partner's tile-r warpgroup writes its rows of the partial result into
+// this CTA's Q tiles (free once this CTA's last Q K^T products completed,
+// which its producer signals to the partner) through distributed shared
+// memory, and this CTA merges the two by the online-softmax rule and writes
+// O and LSE. The last round then takes about half as long (e.g. 512 units on
+// 152 SMs: 3.5 rounds instead of 4).
+//
 // Warp roles (12 warps, 3 warpgroups):
 //   warps 0-3   softmax + epilogue for query tile 0 (one thread per row)
 //   warps 4-7   softmax + epilogue for query tile 1
@@ -110,7 +123,9 @@ struct FwdParams {
   int H_kv;                    // K/V heads; query head h reads K/V head h / (H / H_kv)
   int n_kv_blocks;
   int q_blocks;                // 256-row query blocks per head
-  int num_units;               // B * H * q_blocks: the (b, h, query block) units the CTAs walk
+  int num_units;               // B * H * q_blocks: the (b, h, query block) units
+  int num_whole;               // units walked whole (u = blockIdx.x + k * gridDim.x < num_whole)
+  int split_tail;              // 1: units [num_whole, num_units) are split over CTA pairs (clusters of 2)
   float scale_log2;            // |scale| * log2(e)
   uint32_t idesc_qk;           // instruction descriptor of S = Q K^T (A negated when scale < 0)
   unsigned long long timeout_ns;
@@ -173,6 +188,36 @@ __device__ __forceinline__ bool wait_warp_or_abort(uint32_t bar, uint32_t parity
   }
 }
 
+// wait_warp_or_abort for a barrier that another CTA of the cluster arrives
+// on: the wait acquires at cluster scope, so the data that CTA wrote into
+// this one before arriving is visible when it returns true.
+__device__ __forceinline__ bool wait_cluster_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                      unsigned long long timeout_ns, unsigned int role) {
+  if (__all_sync(0xffffffffu, ptx::mbar_try_wait_cluster(bar, parity))) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  const int lane = threadIdx.x & 31;
+  while (true) {
+    if (__all_sync(0xffffffffu, ptx::mbar_try_wait_cluster(bar, parity))) return true;
+    int stop = 0;
+    if (lane == 0) {
+      if (*abort_flag) {
+        stop = 1;
+      } else if (ptx::globaltimer_ns() - t0 > timeout_ns) {
+        *abort_flag = 1;
+        if (atomicCAS(&g_status_word, 0u, 1u) == 0u) {
+          g_status_info[0] = role;
+          g_status_info[1] = blockIdx.x;
+          g_status_info[2] = blockIdx.y;
+          g_status_info[3] = blockIdx.z;
+        }
+        __threadfence();
+        stop = 1;
+      }
+    }
+    if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+  }
+}
+
 // Bounded wait used only while cleaning up after an abort: ignores the abort
 // flag, gives up silently after `timeout_ns`.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsigned long long timeout_ns) {
@@ -180,6 +225,26 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsign
   while (!ptx::mbar_try_wait(bar, parity)) {
     if (ptx::globaltimer_ns() - t0 > timeout_ns) return;
   }
+}
+
+// The split unit of this CTA's pair and this CTA's half of its key blocks
+// (rank 0 the first ceil(n/2), rank 1 the rest); valid is false when the
+// grid has no split units or this pair has none.
+struct TailPart {
+  uint32_t rank;
+  int u, kb0, kb1;
+  bool valid;
+};
+
+__device__ __forceinline__ TailPart tail_part(const FwdParams& p) {
+  TailPart tp;
+  tp.rank = p.split_tail ? ptx::cluster_ctarank() : 0u;
+  tp.u = p.num_whole + static_cast<int>(blockIdx.x >> 1);
+  tp.valid = p.split_tail && tp.u < p.num_units;
+  const int half = (p.n_kv_blocks + 1) >> 1;
+  tp.kb0 = tp.rank ? half : 0;
+  tp.kb1 = tp.rank ? p.n_kv_blocks : half;
+  return tp;
 }
 
 template <int HD>
@@ -196,6 +261,12 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
   __shared__ __align__(8) uint64_t bar_p_full[2];
   __shared__ __align__(8) uint64_t bar_o_full[2];
   __shared__ __align__(8) uint64_t bar_drain;
+  // Split units: the partner CTA's producer arrives on bar_peer_ready when
+  // its Q tiles may be overwritten; its 128 sending threads arrive on
+  // bar_xfer_full once their rows of the partial result are in this CTA.
+  __shared__ __align__(8) uint64_t bar_peer_ready;
+  __shared__ __align__(8) uint64_t bar_xfer_full;
+  __shared__ float xch_m[C::kBM], xch_l[C::kBM], xch_lo[C::kBM];
   __shared__ uint32_t tmem_base_slot;
   __shared__ int abort_flag;
 
@@ -230,6 +301,8 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
       ptx::mbar_init(ptx::smem_u32(&bar_o_full[t]), 1);
     }
     ptx::mbar_init(ptx::smem_u32(&bar_drain), 1);
+    ptx::mbar_init(ptx::smem_u32(&bar_peer_ready), 1);
+    ptx::mbar_init(ptx::smem_u32(&bar_xfer_full), C::kBM);
     abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -244,8 +317,11 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
   }
   ptx::tc_fence_before();
   __syncthreads();
+  // The partner's barriers must be initialised before any arrival from here.
+  if (p.split_tail) ptx::cluster_sync();
   ptx::tc_fence_after();
   const uint32_t tmem_base = tmem_base_slot;
+
   volatile int* abort_ptr = &abort_flag;
 
   if (warp >= 8) ptx::setmaxnreg_dec<C::kRegsControl>();
@@ -259,7 +335,7 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
       int q_issued = 0;     // Q loads issued (one per unit)
       bool ok = true;
       int uc = 0;
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+      for (int u = blockIdx.x; u < p.num_whole && ok; u += gridDim.x, ++uc) {
         const int bh = unit_head(u), bh_kv = kv_head(bh), q_row0 = unit_row0(u);
         // The previous unit's Q tiles are free once its last Q K^T products completed.
         if (uc > 0 && !wait_or_abort(ptx::smem_u32(&bar_q_empty), (uc - 1) & 1, abort_ptr, p.timeout_ns,
@@ -293,6 +369,45 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
                                j * C::kBN, bh_kv, pol_kv);
           }
         }
+      }
+      if (const TailPart tp = tail_part(p); ok && tp.valid) {
+        // The split unit: Q, then this CTA's half of the key blocks.
+        const int bh = unit_head(tp.u), bh_kv = kv_head(bh), q_row0 = unit_row0(tp.u);
+        if (uc > 0 && !wait_or_abort(ptx::smem_u32(&bar_q_empty), (uc - 1) & 1, abort_ptr, p.timeout_ns,
+                                     kRoleProducer))
+          ok = false;
+        if (ok) {
+          ptx::mbar_arrive_expect_tx(q_full, C::kQTiles * C::kTileBytes);
+          for (int t = 0; t < C::kQTiles; ++t)
+            for (int c = 0; c < C::kChunks; ++c)
+              ptx::tma_load_3d(sQ + t * C::kTileBytes + c * C::kChunkBytes, &tmQ, q_full, c * 64,
+                               q_row0 + t * C::kBM, bh, pol_q);
+          q_issued = uc + 1;
+        }
+        for (int j = tp.kb0; j < tp.kb1 && ok; ++j) {
+          for (int kv = 0; kv < 2; ++kv) {
+            const int it = 2 * n_kv * uc + 2 * (j - tp.kb0) + kv;
+            const int slot = it % C::kStages;
+            const uint32_t phase = (it / C::kStages) & 1;
+            if (!wait_or_abort(ptx::smem_u32(&bar_kv_empty[slot]), phase ^ 1u, abort_ptr, p.timeout_ns,
+                               kRoleProducer)) {
+              ok = false;
+              break;
+            }
+            issued = it + 1;
+            if (it == p.drop_load) continue;   // test hook: this tile never arrives
+            const uint32_t full = ptx::smem_u32(&bar_kv_full[slot]);
+            ptx::mbar_arrive_expect_tx(full, C::kTileBytes);
+            const void* map = kv ? static_cast<const void*>(&tmV) : static_cast<const void*>(&tmK);
+            for (int c = 0; c < C::kChunks; ++c)
+              ptx::tma_load_3d(sKV + slot * C::kTileBytes + c * C::kChunkBytes, map, full, c * 64,
+                               j * C::kBN, bh_kv, pol_kv);
+          }
+        }
+        // Once its Q K^T products have completed, the partner may write its
+        // partial result over this CTA's Q tiles.
+        if (ok && wait_or_abort(ptx::smem_u32(&bar_q_empty), uc & 1, abort_ptr, p.timeout_ns, kRoleProducer))
+          ptx::mbar_arrive_remote(ptx::mapa_shared(ptx::smem_u32(&bar_peer_ready), tp.rank ^ 1u));
       }
       if (!ok || *abort_ptr) {
         // Let every copy this thread started land before the CTA exits.
@@ -341,7 +456,7 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
     // (the phase of s_full / p_full).
     bool ok = true;
     int g = 0, uc = 0;
-    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+    for (int u = blockIdx.x; u < p.num_whole && ok; u += gridDim.x, ++uc) {
       const int it0 = 2 * n_kv * uc;
       ok = wait_warp_or_abort(ptx::smem_u32(&bar_q_full), uc & 1, abort_ptr, p.timeout_ns, kRoleMma);
       if (ok)
@@ -378,6 +493,43 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
         if (t == 1) ptx::mma_commit_warp(ptx::smem_u32(&bar_kv_empty[itV % C::kStages]));
       }
     }
+    if (const TailPart tp = tail_part(p); ok && tp.valid) {
+      // The split unit: the same sequence over this CTA's half of the key blocks.
+      const int it0 = 2 * n_kv * uc;
+      const int nb = tp.kb1 - tp.kb0;
+      ok = wait_warp_or_abort(ptx::smem_u32(&bar_q_full), uc & 1, abort_ptr, p.timeout_ns, kRoleMma);
+      if (ok)
+        ok = wait_warp_or_abort(ptx::smem_u32(&bar_kv_full[it0 % C::kStages]), (it0 / C::kStages) & 1, abort_ptr,
+                                p.timeout_ns, kRoleMma);
+      for (int j = 0; j < nb && ok; ++j, ++g) {
+        const int itK = it0 + 2 * j;
+        ptx::tc_fence_after();
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j > 0) {
+            ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_full[t]), (g - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            issue_pv(t, itK - 1, j > 1);
+            if (t == 1) ptx::mma_commit_warp(ptx::smem_u32(&bar_kv_empty[(itK - 1) % C::kStages]));
+          }
+          issue_qk(t, itK);
+          ptx::mma_commit_warp(ptx::smem_u32(&bar_s_full[t]));
+        }
+        if (ok) {
+          ptx::mma_commit_warp(ptx::smem_u32(&bar_kv_empty[itK % C::kStages]));
+          if (j == nb - 1) ptx::mma_commit_warp(ptx::smem_u32(&bar_q_empty));
+        }
+      }
+      const int itV = it0 + 2 * nb - 1;
+      for (int t = 0; t < 2 && ok; ++t) {
+        ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_full[t]), (g - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        issue_pv(t, itV, nb > 1);
+        ptx::mma_commit_warp(ptx::smem_u32(&bar_o_full[t]));
+        if (t == 1) ptx::mma_commit_warp(ptx::smem_u32(&bar_kv_empty[itV % C::kStages]));
+      }
+    }
     if (!ok) {
       // Wait for every MMA already issued before TMEM is freed.
       ptx::mma_commit_warp(ptx::smem_u32(&bar_drain));
@@ -396,7 +548,7 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
     const float sl2 = p.scale_log2;
     bool ok = true;
     int g = 0, uc = 0;      // key blocks and units so far (barrier phases)
-    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+    for (int u = blockIdx.x; u < p.num_whole && ok; u += gridDim.x, ++uc) {
     const int it0 = 2 * n_kv * uc;
     float m_use = 0.f;      // raw-score maximum the exponentials are taken against
     float l = 0.f;          // running sum of exp, relative to m_use (for LSE)
@@ -556,6 +708,202 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
       }
     }
     }   // units
+    if (const TailPart tp = tail_part(p); ok && tp.valid) {
+      // The split unit: the block loop over this CTA's half of the keys, then
+      // the exchange with the partner.
+      const int it0 = 2 * n_kv * uc;
+      float m_use = 0.f, l = 0.f, lo = 0.f;
+      for (int j = tp.kb0; j < tp.kb1; ++j, ++g) {
+        // V_j and K_{j+1} must have landed before this block's hand-off (see
+        // the MMA issuer); waiting here costs nothing, S_t(j) comes later.
+        {
+          const int itV = it0 + 2 * (j - tp.kb0) + 1;
+          ok = wait_warp_or_abort(ptx::smem_u32(&bar_kv_full[itV % C::kStages]), (itV / C::kStages) & 1, abort_ptr,
+                                  p.timeout_ns, kRoleSoftmax);
+          if (ok && j + 1 < tp.kb1)
+            ok = wait_warp_or_abort(ptx::smem_u32(&bar_kv_full[(itV + 1) % C::kStages]), ((itV + 1) / C::kStages) & 1,
+                                    abort_ptr, p.timeout_ns, kRoleSoftmax);
+          if (!ok) break;
+        }
+        ok = wait_warp_or_abort(ptx::smem_u32(&bar_s_full[t]), g & 1, abort_ptr, p.timeout_ns, kRoleSoftmax);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        // The loads also reduce each 32-column piece to its maximum, which is
+        // the row maximum of a full block. In the ragged last block the
+        // columns past N hold scores of zero-filled keys, so that block masks
+        // them to -inf and takes the maximum itself.
+        uint32_t s[4][32];
+        float mr[4];
+  #pragma unroll
+        for (int c = 0; c < 4; ++c) ptx::tmem_ld32_max(tS + 32 * c, s[c], mr[c]);
+        ptx::tmem_ld_wait();
+  #pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          ptx::reg_fence32(s[c]);
+          ptx::reg_fence1(mr[c]);
+        }
+
+        const int valid = p.N_kv - j * C::kBN;    // keys of this block that exist
+        const bool ragged = valid < C::kBN;
+        float mt;
+        if (!ragged) {
+          mt = ptx::max3(mr[0], mr[1], fmaxf(mr[2], mr[3]));
+        } else {
+  #pragma unroll
+          for (int c = 0; c < 4; ++c)
+  #pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (32 * c + i >= valid) s[c][i] = __float_as_uint(-INFINITY);
+          // Row maximum: 8 independent chains of 3-input max, then a small tree.
+          float mc[8];
+  #pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int c = k >> 1, b = (k & 1) * 16;
+            mc[k] = fmaxf(__uint_as_float(s[c][b]), __uint_as_float(s[c][b + 1]));
+  #pragma unroll
+            for (int i = 2; i < 16; i += 2)
+              mc[k] = ptx::max3(mc[k], __uint_as_float(s[c][b + i]), __uint_as_float(s[c][b + i + 1]));
+          }
+          mt = ptx::max3(ptx::max3(mc[0], mc[1], mc[2]), ptx::max3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
+        }
+
+        float alpha = 1.f;
+        bool rescale_o = false;
+        if (j == tp.kb0) {
+          m_use = mt;
+        } else {
+          const bool need = (mt - m_use) * sl2 > kRescaleLog2;
+          rescale_o = __any_sync(0xffffffffu, need);
+          if (need) {
+            alpha = ptx::ex2_approx((m_use - mt) * sl2);
+            m_use = mt;
+          }
+        }
+        // P = 2^(s*scale*log2e - m*scale*log2e): pairs through the f32x2 FMA,
+        // MUFU ex2 per element, 4 independent f32x2 partial sums, bf16x2 pack.
+        const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
+        const float neg_m = -m_use * sl2;
+        const uint64_t negmx2 = ptx::f2_pack(neg_m, neg_m);
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+        uint32_t pk[2][32];
+  #pragma unroll
+        for (int c = 0; c < 4; ++c) {
+  #pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float x0, x1;
+            ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[c][i]), __uint_as_float(s[c][i + 1])), sl2x2,
+                                       negmx2),
+                           x0, x1);
+            float p0 = ptx::ex2_approx(x0);
+            float p1 = ptx::ex2_approx(x1);
+            if (ragged) {   // exact zeros for keys past N (also when scale == 0)
+              if (32 * c + i >= valid) p0 = 0.f;
+              if (32 * c + i + 1 >= valid) p1 = 0.f;
+            }
+            acc[(i >> 1) & 3] = ptx::f2_add(acc[(i >> 1) & 3], ptx::f2_pack(p0, p1));
+            pk[c >> 1][(c & 1) * 16 + (i >> 1)] = ptx::pack_bf16x2(p0, p1);
+          }
+        }
+        float sum;
+        {
+          float a0, a1, b0, b1;
+          ptx::f2_unpack(ptx::f2_add(acc[0], acc[1]), a0, a1);
+          ptx::f2_unpack(ptx::f2_add(acc[2], acc[3]), b0, b1);
+          sum = (a0 + a1) + (b0 + b1);
+        }
+        // The P V product sees every probability rounded to bf16. The largest
+        // one of the block (the score equal to mt, recomputed here exactly as
+        // the loop above computes it) enters the normaliser of O the same way,
+        // so that a row dominated by one key weights it exactly 1; l itself,
+        // which LSE needs, stays the sum of the unrounded terms.
+        const float pmax = ptx::ex2_approx(fmaf(mt, sl2, neg_m));
+        l = l * alpha + sum;
+        lo = lo * alpha + (sum + (ptx::round_bf16(pmax) - pmax));
+        ptx::tmem_st32(tS, pk[0]);
+        ptx::tmem_st32(tS + 32, pk[1]);
+        if (rescale_o) {
+  #pragma unroll
+          for (int c = 0; c < HD / 32; ++c) {
+            uint32_t o[32];
+            ptx::tmem_ld32(tO + 32 * c, o);
+            ptx::tmem_ld_wait();
+            ptx::reg_fence32(o);
+  #pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            ptx::tmem_st32(tO + 32 * c, o);
+          }
+        }
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(ptx::smem_u32(&bar_p_full[t]));
+      }
+      if (ok) ok = wait_warp_or_abort(ptx::smem_u32(&bar_o_full[t]), uc & 1, abort_ptr, p.timeout_ns, kRoleSoftmax);
+      const int bh = unit_head(tp.u);
+      const int grow = unit_row0(tp.u) + t * C::kBM + row;
+      if (ok && t != static_cast<int>(tp.rank)) {
+        // The tile the partner finalises: send this CTA's partial result for
+        // it (unnormalised O relative to m_use, and m_use, l, lo) into the
+        // partner's Q tiles (free once its producer says so), as float32
+        // [d][128 rows], then arrive on its bar_xfer_full.
+        ok = wait_cluster_or_abort(ptx::smem_u32(&bar_peer_ready), 0, abort_ptr, p.timeout_ns, kRoleSoftmax);
+        if (ok) {
+          ptx::tc_fence_after();
+          const uint32_t peer = tp.rank ^ 1u;
+          const uint32_t dst = ptx::mapa_shared(sQ, peer) + static_cast<uint32_t>(row) * 4u;
+#pragma unroll 1
+          for (int c = 0; c < HD / 8; ++c) {
+            uint32_t o[8];
+            ptx::tmem_ld8(tO + 8 * c, o);
+            ptx::tmem_ld_wait();
+            ptx::reg_fence8(o);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              ptx::st_shared_cluster_f32(dst + static_cast<uint32_t>((8 * c + i) * C::kBM * 4), __uint_as_float(o[i]));
+          }
+          ptx::st_shared_cluster_f32(ptx::mapa_shared(ptx::smem_u32(&xch_m[row]), peer), m_use);
+          ptx::st_shared_cluster_f32(ptx::mapa_shared(ptx::smem_u32(&xch_l[row]), peer), l);
+          ptx::st_shared_cluster_f32(ptx::mapa_shared(ptx::smem_u32(&xch_lo[row]), peer), lo);
+          ptx::mbar_arrive_remote(ptx::mapa_shared(ptx::smem_u32(&bar_xfer_full), peer));
+        }
+      } else if (ok) {
+        // The tile this CTA finalises: merge the partner's partial result
+        // over the other half of the keys with this CTA's ("Flash Attention
+        // (FA1)", derivation steps 4-5): with m = max(m_a, m_b) and
+        // a_x = 2^{scale log2(e) (m_x - m)}, O = a_a O_a + a_b O_b, and l, lo
+        // alike.
+        ok = wait_cluster_or_abort(ptx::smem_u32(&bar_xfer_full), 0, abort_ptr, p.timeout_ns, kRoleSoftmax);
+        if (ok) {
+          ptx::tc_fence_after();
+          const bool in_range = grow < p.N;
+          __nv_bfloat16* orow = p.O + (static_cast<size_t>(bh) * p.N + grow) * HD;
+          const float m_b = xch_m[row];
+          const float m = fmaxf(m_use, m_b);
+          const float a_a = ptx::ex2_approx((m_use - m) * sl2);
+          const float a_b = ptx::ex2_approx((m_b - m) * sl2);
+          const float l_all = a_a * l + a_b * xch_l[row];
+          const float inv_l = 1.f / (a_a * lo + a_b * xch_lo[row]);
+          const float* part = reinterpret_cast<const float*>(smem_raw + (sQ - ptx::smem_u32(smem_raw)));
+#pragma unroll 1
+          for (int c = 0; c < HD / 8; ++c) {
+            uint32_t o[8];
+            ptx::tmem_ld8(tO + 8 * c, o);
+            ptx::tmem_ld_wait();
+            ptx::reg_fence8(o);
+            uint32_t packed[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float x0 = fmaf(a_a, __uint_as_float(o[2 * i]), a_b * part[(8 * c + 2 * i) * C::kBM + row]);
+              const float x1 = fmaf(a_a, __uint_as_float(o[2 * i + 1]), a_b * part[(8 * c + 2 * i + 1) * C::kBM + row]);
+              packed[i] = ptx::pack_bf16x2(x0 * inv_l, x1 * inv_l);
+            }
+            if (in_range)
+              *reinterpret_cast<uint4*>(orow + 8 * c) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+          }
+          if (in_range)
+            p.LSE[static_cast<size_t>(bh) * p.N + grow] = (m * sl2 + __log2f(l_all)) * 0.69314718055994530942f;
+        }
+      }
+    }
   }
 
   ptx::tc_fence_before();
@@ -564,6 +912,9 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, C::kTmemCols);
   }
+  // Neither CTA of a pair exits while the other may still write into it.
+  // Every wait above is bounded, so every thread of both CTAs gets here.
+  if (p.split_tail) ptx::cluster_sync();
 }
 
 }  // namespace fa
