@@ -12,7 +12,9 @@
 //   bwd_prep_kernel     per query row: -D and -LSE*log2(e) into a workspace
 //                       whose rows are padded to a multiple of 128; padding
 //                       rows get 0 and -inf, so their probabilities are zero.
-//   fa_bwd_kernel       CTAs of two roles:
+//   fa_bwd_kernel       CTAs of two roles, grouped by head (a head's
+//                       key-block CTAs, then its query-block CTAs, so that
+//                       both roles find the head's tiles in L2):
 //     key block (bwd_dkdv_cta)   one CTA per 128 key rows of one (b, h),
 //                       streaming the Q/dO blocks: S^T = K Q_i^T,
 //                       dP^T = V dO_i^T, P^T, dS^T, dV += P^T dO_i,
@@ -529,13 +531,14 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const uint64_t pol_once = ptx::policy_evict_first();
+      // Every tile this CTA loads is read by other CTAs of its head too: its
+      // K and V by the head's query-block CTAs, which run right after it.
       const uint64_t pol_shared = ptx::policy_evict_last();
       const uint32_t kv_full = ptx::smem_u32(&bar_kv_full);
       ptx::mbar_arrive_expect_tx(kv_full, C::kPairBytes);
       for (int c = 0; c < C::kChunks; ++c) {
-        ptx::tma_load_3d(sK + c * C::kChunkBytes, &tmK, kv_full, c * 64, kv0, bh, pol_once);
-        ptx::tma_load_3d(sV + c * C::kChunkBytes, &tmV, kv_full, c * 64, kv0, bh, pol_once);
+        ptx::tma_load_3d(sK + c * C::kChunkBytes, &tmK, kv_full, c * 64, kv0, bh, pol_shared);
+        ptx::tma_load_3d(sV + c * C::kChunkBytes, &tmV, kv_full, c * 64, kv0, bh, pol_shared);
       }
       // Q_i (with its rows' -LSE*log2e) goes into its slot as soon as dK of
       // the slot's previous block has completed, dO_i (with -D) once dV has:
@@ -752,12 +755,15 @@ __global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                   const BwdParams p) {
-  const long long per_role = static_cast<long long>(p.n_blocks) * p.BH;
-  long long idx = blockIdx.x;
-  const bool dkdv = idx < per_role;
-  if (!dkdv) idx -= per_role;
-  const int blk = static_cast<int>(idx % p.n_blocks);
-  const int bh = static_cast<int>(idx / p.n_blocks);
+  // The CTAs of one head are consecutive: its key-block CTAs (the longer
+  // role first), then its query-block CTAs. Both roles stream that head's Q,
+  // K, V and dO, which then stay in L2 from one role to the other.
+  const long long per_head = 2LL * p.n_blocks;
+  const long long idx = blockIdx.x;
+  const int bh = static_cast<int>(idx / per_head);
+  const int r = static_cast<int>(idx - bh * per_head);
+  const bool dkdv = r < p.n_blocks;
+  const int blk = dkdv ? r : r - p.n_blocks;
   if (dkdv)
     bwd_dkdv_cta<HD>(tmQ, tmK, tmV, tmdO, p, blk, bh);
   else
