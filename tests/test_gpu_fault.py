@@ -82,3 +82,27 @@ def test_backward_fault_hook_rejects_zero_timeout():
     ws = torch.empty(fa.fa_bwd_workspace_bytes(1, 1, 128), dtype=torch.uint8, device="cuda")
     g = [torch.zeros_like(q) for _ in range(3)]
     assert fa.fa_bwd_fault_test(q, k, v, q.clone(), q.clone(), lse, *g, 0.125, ws, 0, 0) == fa.FA_ERR_INVALID_ARG
+
+
+def test_dropped_load_in_a_split_unit_times_out_cleanly():
+    """160 units (40 heads of 1024 rows): one whole round, then 8 units shared by
+    CTA pairs. Load 20 of a CTA is a K/V tile of its shared unit, so that
+    CTA's wait runs out, its partner's waits for the exchange run out too, and
+    both still meet at the closing cluster barrier: the launch ends with a
+    timeout status and the next call is correct."""
+    B, H, N, d = 1, 40, 1024, 128
+    q, k, v = inputs.make_random(B, H, N, d, seed=60)
+    qd, kd, vd = (x.cuda() for x in (q, k, v))
+    o = torch.zeros_like(qd)
+    lse = torch.zeros(B, H, N, dtype=torch.float32, device="cuda")
+    assert fa.fa_fwd_fault_test(qd, kd, vd, o, lse, 1 / math.sqrt(d), 20, 20_000_000) == fa.FA_OK
+    st, info = fa.fa_get_device_status()
+    assert st == fa.FA_ERR_TIMEOUT, (st, info)
+    assert info[0] in (1, 2, 3)
+    s = 1 / math.sqrt(d)
+    o2, lse2 = fa.fa_fwd(qd, kd, vd, scale=s)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status()[0] == fa.FA_OK
+    O_ref, L_ref = oracle.attention(*(parity.to64(x) for x in (q, k, v)), s)
+    err = parity.errors(o2.cpu(), lse2.cpu(), O_ref, L_ref)
+    assert err["o_max"] <= parity.TOL_O_MAX and err["lse_max"] <= parity.TOL_LSE_MAX, err

@@ -222,3 +222,23 @@ def test_negative_scale_equals_negated_keys(d):
     o2, l2 = parity.run_gpu(q, -k, v, 0.09)
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
     assert torch.equal(l1, l2)
+
+
+# --- units shared by CTA pairs (the split last round) ----------------------------
+@pytest.mark.parametrize("d", [64, 128])
+def test_whole_rounds_then_split_tail(d):
+    """40 heads of 1024 rows are 160 units of 256 rows: one whole round on the
+    SMs, then 8 units each shared by a pair of CTAs (half of the 8 key blocks
+    each, merged through distributed shared memory). Every row against the
+    oracle."""
+    q, k, v = inputs.make_random(1, 40, 1024, d, seed=50 + d)
+    err, _, _ = parity.check_full(q, k, v, 1 / math.sqrt(d))
+    print(d, err)
+
+
+def test_split_units_with_ragged_keys_and_negative_scale():
+    """Split units where the second half ends in a ragged key block, with a
+    negative scale (the scores negated on the tensor core)."""
+    q, k, v = inputs.make_random(2, 3, 777, 128, seed=53)
+    err, _, _ = parity.check_full(q, k, v, -0.07)
+    print(err)
