@@ -68,6 +68,12 @@ typedef enum {
  *   stream  : CUDA stream the kernel is enqueued on (0 = legacy default).
  * Returns FA_OK once the kernel is enqueued; otherwise an error code and
  * nothing is launched (FA_ERR_CUDA: the launch itself failed).
+ * The launch is a persistent grid of at most one CTA per SM walking units of
+ * 256 query rows; when the units of its last, partial round fill at most
+ * half of the SMs, it is launched as clusters of two CTAs that share those
+ * units (half of the key blocks each, merged on chip). The result does not
+ * depend on the stream or on other work on the GPU, but it does depend on
+ * the SM count (which units are shared), like any reduction order.
  * Follows: "Flash Attention (FA1)" tiling and online-softmax update;
  * "01 · 注意力为什么是 IO 瓶颈" §4/§6 for the O + LSE outputs.
  */
