@@ -89,9 +89,20 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 
+// Units [0, whole_units) of a problem of total_units units run whole; the rest
+// (the last, partial round) are shared by CTA pairs. A launch covering only
+// part of the problem (unit_offset onwards, e.g. one head group of
+// fa_fwd_host) follows the whole problem's plan, so that every unit is
+// computed the same way as by one launch over everything.
+struct SplitPlan {
+  int total_units;
+  int unit_offset;
+};
+
 template <int HD>
 fa_status_t launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int H_kv, int N,
-                   int N_kv, float scale, int drop_load, unsigned long long timeout_ns, cudaStream_t stream) {
+                   int N_kv, float scale, int drop_load, unsigned long long timeout_ns, cudaStream_t stream,
+                   const SplitPlan* plan = nullptr) {
   using C = fa::FwdCfg<HD>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -147,13 +158,20 @@ fa_status_t launch(const void* Q, const void* K, const void* V, void* O, float* 
   p.num_whole = p.num_units;
   p.split_tail = 0;
   const int even = sms & ~1;
+  const int total = plan ? plan->total_units : p.num_units;
+  const int offset = plan ? plan->unit_offset : 0;
   if (p.n_kv_blocks >= 4 && even >= 2) {   // at least two key blocks for each half
-    const int whole = p.num_units / even;
-    const int tail = p.num_units - whole * even;
+    const int whole = total / even;
+    const int tail = total - whole * even;
     if (tail > 0 && 2 * tail <= even) {
-      p.split_tail = 1;
-      p.num_whole = whole * even;
-      grid = even;
+      // This launch's units past the problem's whole rounds are shared; they
+      // are a suffix of its units and at most half the grid.
+      const int local_whole = std::max(0, std::min(p.num_units, whole * even - offset));
+      if (local_whole < p.num_units) {
+        p.split_tail = 1;
+        p.num_whole = local_whole;
+        grid = even;
+      }
     }
   }
   if (p.split_tail) {
@@ -485,6 +503,8 @@ fa_status_t host_impl(const void* Qh, const void* Kh, const void* Vh, void* Oh, 
   const int per = (BH + nc - 1) / nc;
   const size_t head_bytes = static_cast<size_t>(N) * d * 2;
   const size_t head_lse = static_cast<size_t>(N) * 4;
+  constexpr int kUnitRows = fa::FwdCfg<128>::kQTiles * fa::FwdCfg<128>::kBM;   // rows per unit (either d)
+  const int q_blocks = (N + kUnitRows - 1) / kUnitRows;
 
   std::lock_guard<std::mutex> lock(hp->mu);
 #define FA_TRY(x)                              \
@@ -512,11 +532,13 @@ fa_status_t host_impl(const void* Qh, const void* Kh, const void* Vh, void* Oh, 
     FA_TRY(cudaStreamWaitEvent(cs, hp->in[c], 0));
     // The chunk's heads as a [1, nbh, N, d] problem: the same kernel and the
     // same per-head result as fa_fwd.
+    // (with the whole problem's plan for the units CTA pairs share)
+    const SplitPlan plan{BH * q_blocks, bh0 * q_blocks};
     const fa_status_t st =
         d == 64 ? launch<64>(Qd + off, Kd + off, Vd + off, Od + off, reinterpret_cast<float*>(Ld + loff), 1, nbh,
-                             nbh, N, N, scale, -1, kDefaultTimeoutNs, cs)
+                             nbh, N, N, scale, -1, kDefaultTimeoutNs, cs, &plan)
                 : launch<128>(Qd + off, Kd + off, Vd + off, Od + off, reinterpret_cast<float*>(Ld + loff), 1, nbh,
-                              nbh, N, N, scale, -1, kDefaultTimeoutNs, cs);
+                              nbh, N, N, scale, -1, kDefaultTimeoutNs, cs, &plan);
     if (st != FA_OK) return st;
     FA_TRY(cudaEventRecord(hp->done[c], cs));
     FA_TRY(cudaStreamWaitEvent(hp->down, hp->done[c], 0));

@@ -91,7 +91,9 @@ size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d);
  * fa_fwd_host -- fa_fwd on HOST buffers, end to end: uploads Q, K, V, runs the
  * forward kernel and downloads O and LSE, pipelined over groups of (b, h)
  * heads so that the uploads of one group and the downloads of another overlap
- * the kernel on a third. Each head's O and LSE are bit for bit those of fa_fwd.
+ * the kernel on a third. Each head's O and LSE are bit for bit those of fa_fwd
+ * (the group launches follow the whole problem's choice of the units CTA
+ * pairs share).
  *   Qh, Kh, Vh : host, bf16 [B, H, N, d], read. Page-locked (pinned) memory
  *                gives full copy bandwidth; pageable memory works, slower.
  *   Oh, LSEh   : host, bf16 [B, H, N, d] and float32 [B, H, N], written.

@@ -148,3 +148,16 @@ def test_host_path_negative_scale():
     od, ld = parity.run_gpu(q, k, v, -0.1)
     assert bits_equal(oh, od)
     assert torch.equal(lh, ld)
+
+
+@pytest.mark.parametrize("num_chunks", [3, 7, 16])
+def test_host_groups_follow_the_whole_problems_shared_units(num_chunks):
+    """40 heads of 1024 rows: fa_fwd runs one whole round of units and has CTA
+    pairs share the last 8 (heads 38 and 39). The head groups of fa_fwd_host are
+    separate launches with fewer units each; they still share exactly those
+    units, so every head's result is fa_fwd's, bit for bit."""
+    q, k, v = inputs.make_random(1, 40, 1024, 128, seed=91)
+    oh, lh = run_host(q, k, v, 0.088, num_chunks=num_chunks)
+    od, ld = parity.run_gpu(q, k, v, 0.088)
+    assert bits_equal(oh, od)
+    assert torch.equal(lh, ld)
