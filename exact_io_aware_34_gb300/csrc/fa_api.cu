@@ -789,11 +789,18 @@ fa_status_t decode_launch(const void* Q, const void* K, const void* V, void* O, 
   if (dev < 0 || dev >= 64) return FA_ERR_UNSUPPORTED;
   static std::once_flag once[64];
   static cudaError_t attr_err[64];
+  static bool regs_ok[64];
   std::call_once(once[dev], [&] {
     attr_err[dev] =
         cudaFuncSetAttribute(fa::fa_decode_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    // The warpgroups' register split must fit the registers the block is
+    // launched with (see the forward launch).
+    cudaFuncAttributes fattr;
+    if (attr_err[dev] == cudaSuccess) attr_err[dev] = cudaFuncGetAttributes(&fattr, fa::fa_decode_kernel<HD>);
+    regs_ok[dev] = attr_err[dev] == cudaSuccess && 4 * C::kRegsSoftmax + 4 * C::kRegsControl <= 8 * fattr.numRegs;
   });
   if (attr_err[dev] != cudaSuccess) return cuda_fail(attr_err[dev]);
+  if (!regs_ok[dev]) return FA_ERR_UNSUPPORTED;
 
   // Q as [B*H][N_q][d] with a box of 64 x N_q rows x hp heads: one load
   // brings the packed rows of hp query heads. K, V as [B*H_kv][N_kv][d].

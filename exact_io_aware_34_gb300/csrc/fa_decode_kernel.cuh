@@ -22,9 +22,13 @@
 //    LSE = ln sum_s e^{LSE_s}, O = sum_s e^{LSE_s - LSE} O_s.
 //    With one split the CTA writes O and LSE directly.
 //
-// Per CTA (192 threads): warps 0-3 run the softmax and epilogue of the one
-// tile (one thread per row), warp 4 is the TMA producer, warp 5 allocates
-// TMEM and issues the MMAs (converged, one elected lane issuing). TMEM: S at
+// Per CTA (256 threads, 2 warpgroups): warps 0-3 run the softmax and
+// epilogue of the one tile (one thread per row), warp 4 is the TMA producer,
+// warp 5 allocates TMEM and issues the MMAs (converged, one elected lane
+// issuing), warps 6-7 are idle. Two CTAs per SM launch with 128 registers per
+// thread; setmaxnreg moves registers from the control warpgroup (down to 56)
+// to the softmax warpgroup (up to 200), which then holds a 128-score row and
+// its packed probabilities without spilling. TMEM: S at
 // column 0 (P, packed bf16, over its
 // first 64 columns), O at column 128. The per-block update is the forward
 // kernel's, including the lazy rescale. With a single tile, a CTA's QK^T,
@@ -49,7 +53,15 @@ struct DecCfg {
   static constexpr int kStages = (HD == 128) ? 2 : 4;      // K/V ring slots
   static constexpr int kCtasPerSm = 2;                       // 2 x (Q + ring) fits shared memory, 2 x 256 TMEM
   static constexpr int kSmemBytes = kTileBytes + kStages * kTileBytes + 1024;
-  static constexpr int kThreads = 192;
+  static constexpr int kThreads = 256;                       // 8 warps: 2 warpgroups
+  // Registers per thread after the split: the softmax warpgroup raises its
+  // own, the control warpgroup (producer, MMA issuer, two idle warps) lowers
+  // its own. Two CTAs per SM launch with 128 registers per thread; the split
+  // must not need more (the host checks the built kernel's count).
+  static constexpr int kRegsLaunch = 128;
+  static constexpr int kRegsSoftmax = 200;
+  static constexpr int kRegsControl = 56;
+  static_assert(4 * kRegsSoftmax + 4 * kRegsControl <= 8 * kRegsLaunch, "register split exceeds the launch");
   static constexpr uint32_t kTmemCols = 256;
   static constexpr uint32_t kColS = 0;
   static constexpr uint32_t kColO = 128;
@@ -155,6 +167,7 @@ __global__ void __launch_bounds__(DecCfg<HD>::kThreads, DecCfg<HD>::kCtasPerSm)
   const uint32_t tmem_base = tmem_base_slot;
   volatile int* abort_ptr = &abort_flag;
 
+  if (warp >= 4) ptx::setmaxnreg_dec<C::kRegsControl>();
   if (warp == 4) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -250,8 +263,9 @@ __global__ void __launch_bounds__(DecCfg<HD>::kThreads, DecCfg<HD>::kCtasPerSm)
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp < 4) {
     // ------------------------------------------------------------ softmax + epilogue
+    ptx::setmaxnreg_inc<C::kRegsSoftmax>();
     const int quarter = warp;
     const int row = quarter * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
