@@ -392,8 +392,8 @@ fa_status_t bwd_launch(const void* Q, const void* K, const void* V, const void* 
   p.timeout_ns = timeout_ns;
   p.drop_load = drop_load;
 
-  // 1. -LSE*log2(e) and -D per query row (one warp each, 8 per block)
-  fa::bwd_prep_kernel<HD><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
+  // 1. -LSE*log2(e) and -D per query row (eight rows per warp, 64 per block)
+  fa::bwd_prep_kernel<HD><<<static_cast<unsigned>((rows + 63) / 64), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), LSE, static_cast<float*>(ws),
       static_cast<float*>(ws) + rows, N, p.Npad, rows);
   e = cudaGetLastError();

@@ -98,50 +98,70 @@ struct BwdParams {
 };
 
 // ---------------------------------------------------------------- prep
-// One warp per padded query row: D = dO_r . O_r (float32 sum of the exact
-// products of bf16 values) and LSE_r * log2(e), stored negated.
+// Eight padded query rows per warp: D = dO_r . O_r (float32 sum of the exact
+// products of bf16 values) and LSE_r * log2(e), both stored negated. A row is
+// read as 16-byte pieces, HD / 8 lanes to a row, and every piece of the
+// warp's rows is requested before the first product so that each warp keeps
+// 4 KB (d = 128) of loads in flight.
 template <int HD>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ O,
                                                        const __nv_bfloat16* __restrict__ dO,
                                                        const float* __restrict__ LSE, float* __restrict__ nlse2,
                                                        float* __restrict__ ndelta, int N, int Npad,
                                                        long long rows) {
-  const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  constexpr int kRowsPerWarp = 8;
+  constexpr int kLanesPerRow = HD / 8;                       // 16-byte pieces per row: 16 or 8
+  constexpr int kRowsPerLoad = 32 / kLanesPerRow;            // rows one warp-wide load covers: 2 or 4
+  constexpr int kLoads = kRowsPerWarp / kRowsPerLoad;        // loads per lane per operand: 4 or 2
+  static_assert(kLanesPerRow * kRowsPerLoad == 32 && kLoads * kRowsPerLoad == kRowsPerWarp, "row split");
+  const long long row0 = ((static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * kRowsPerWarp;
+  if (row0 >= rows) return;
   const int lane = threadIdx.x & 31;
-  if (gw >= rows) return;
-  const long long bh = gw / Npad;
-  const int r = static_cast<int>(gw - bh * Npad);
-  float dsum = 0.f;
-  float nl = -INFINITY;
-  if (r < N) {
-    constexpr int kPer = HD / 32;     // elements per lane: 4 (8 bytes) or 2 (4 bytes)
-    const size_t off = (static_cast<size_t>(bh) * N + r) * HD + lane * kPer;
-    __nv_bfloat162 o2[kPer / 2], g2[kPer / 2];
-    if constexpr (kPer == 4) {
-      const uint2 a = *reinterpret_cast<const uint2*>(O + off);
-      const uint2 b = *reinterpret_cast<const uint2*>(dO + off);
-      o2[0] = *reinterpret_cast<const __nv_bfloat162*>(&a.x);
-      o2[1] = *reinterpret_cast<const __nv_bfloat162*>(&a.y);
-      g2[0] = *reinterpret_cast<const __nv_bfloat162*>(&b.x);
-      g2[1] = *reinterpret_cast<const __nv_bfloat162*>(&b.y);
-    } else {
-      o2[0] = *reinterpret_cast<const __nv_bfloat162*>(O + off);
-      g2[0] = *reinterpret_cast<const __nv_bfloat162*>(dO + off);
-    }
+  const int sub = lane / kLanesPerRow, piece = lane % kLanesPerRow;
+  uint4 o4[kLoads], g4[kLoads];
+  float lse[kLoads];
+  bool live[kLoads];
 #pragma unroll
-    for (int e = 0; e < kPer / 2; ++e) {
-      const float2 of = __bfloat1622float2(o2[e]);
-      const float2 gf = __bfloat1622float2(g2[e]);
-      dsum = fmaf(of.x, gf.x, dsum);
-      dsum = fmaf(of.y, gf.y, dsum);
+  for (int i = 0; i < kLoads; ++i) {
+    const long long row = row0 + i * kRowsPerLoad + sub;
+    const long long bh = row / Npad;
+    const int r = static_cast<int>(row - bh * Npad);
+    live[i] = row < rows && r < N;
+    o4[i] = g4[i] = make_uint4(0u, 0u, 0u, 0u);
+    lse[i] = 0.f;
+    if (live[i]) {
+      const size_t off = (static_cast<size_t>(bh) * N + r) * HD + piece * 8;
+      o4[i] = __ldg(reinterpret_cast<const uint4*>(O + off));
+      g4[i] = __ldg(reinterpret_cast<const uint4*>(dO + off));
+      if (piece == 0) lse[i] = __ldg(LSE + static_cast<size_t>(bh) * N + r);
     }
-#pragma unroll
-    for (int s = 16; s > 0; s >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, s);
-    nl = -LSE[static_cast<size_t>(bh) * N + r] * 1.4426950408889634074f;
   }
-  if (lane == 0) {
-    nlse2[gw] = nl;
-    ndelta[gw] = -dsum;
+  float dsum[kLoads];
+#pragma unroll
+  for (int i = 0; i < kLoads; ++i) {
+    const uint32_t ow[4] = {o4[i].x, o4[i].y, o4[i].z, o4[i].w};
+    const uint32_t gw[4] = {g4[i].x, g4[i].y, g4[i].z, g4[i].w};
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[e]));
+      const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[e]));
+      acc = fmaf(of.x, gf.x, acc);
+      acc = fmaf(of.y, gf.y, acc);
+    }
+#pragma unroll
+    for (int s = kLanesPerRow / 2; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    dsum[i] = acc;
+  }
+  if (piece == 0) {
+#pragma unroll
+    for (int i = 0; i < kLoads; ++i) {
+      const long long row = row0 + i * kRowsPerLoad + sub;
+      if (row < rows) {
+        nlse2[row] = live[i] ? -lse[i] * 1.4426950408889634074f : -INFINITY;
+        ndelta[row] = -dsum[i];
+      }
+    }
   }
 }
 
