@@ -496,6 +496,14 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------------------- native arm
+def launch_shape(fa, shape):
+    """The forward's launch for a [B, H, N, d] problem on this device: CTAs,
+    CTAs per cluster (1, or 2 when pairs share the last round's units) and
+    the units of 256 query rows run whole."""
+    g, c, wu = fa.fa_fwd_launch_shape(*shape)
+    return {"grid": g, "cluster": c, "whole_units": wu}
+
+
 def time_forward(fa, qd, kd, vd, o, lse, scale, flush, stream, steps, warmup, local, uuid):
     """``steps`` fa_fwd calls, each bracketed by CUDA events on ``stream`` with the
     L2 cache flushed before it (outside the events); returns (per-step ms, clocks)."""
@@ -621,7 +629,8 @@ def run_native(args):
                              "frac_of_sustained": c_val / peaks_pc["bf16_tflops_sustained"],
                              "peak_source": f"{peak_src_pc} dense bf16 burst",
                              "traffic": load_traffic(cw.name),
-                             "kernel": f"fa_fwd_kernel<{cw.d}>", "flops_per_launch": cw.flops,
+                             "kernel": f"fa_fwd_kernel<{cw.d}>", "launch": launch_shape(fa, tuple(cqd.shape)),
+                             "flops_per_launch": cw.flops,
                              "algorithmic_bytes_per_launch": cw.B * cw.H * cw.N * (8 * cw.d + 4)},
                 "gpu_launches": n_steps,
                 "l2": "flushed before every step (512 MB write, outside the events)",
@@ -797,7 +806,8 @@ def run_native(args):
                          "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
                          "peak_source": f"{peak_src} dense bf16 burst",
                          "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
-                         "kernel": f"fa_fwd_kernel<{d}>", "flops_per_launch": flops,
+                         "kernel": f"fa_fwd_kernel<{d}>", "launch": launch_shape(fa, tuple(qd.shape)),
+                         "flops_per_launch": flops,
                          "algorithmic_bytes_per_launch": B * H * N * (8 * d + 4)},
             "e2e": {"value": job_flops * e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / e2e_steps,

@@ -89,6 +89,79 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 
+// Launch shape of the forward over `units` units of 256 query rows with
+// n_kv key blocks each, on `sms` SMs of which at most `max2` clusters of two
+// can be resident at once (a cluster must fit in one GPC). All units cost
+// the same, so a grid of G CTAs takes ceil(units / G) rounds. When the units
+// left after the whole rounds fill at most half of an even grid, clusters of
+// two share them, one unit per pair, half of its key blocks each: the last
+// round then takes about half as long (512 units on 152 SMs: 3.5 rounds
+// instead of 4). A persistent grid must be resident as a whole, so a
+// clustered grid has at most 2 * max2 CTAs, and it is used only when it
+// takes fewer rounds; each half must hold at least two key blocks.
+struct FwdShape {
+  int grid, cluster, whole_units;
+};
+FwdShape fwd_shape(int units, int n_kv, int sms, int max2) {
+  const int g1 = std::max(1, std::min(units, sms));
+  const FwdShape plain{g1, 1, units};
+  const int g2 = std::min(sms & ~1, 2 * max2);
+  if (n_kv < 4 || g2 < 2) return plain;
+  const int whole = units / g2 * g2, tail = units - whole;
+  if (tail == 0 || 2 * tail > g2) return plain;
+  // whole / g2 + 1/2 rounds against ceil(units / g1)
+  return 2 * (whole / g2) + 1 < 2 * ((units + g1 - 1) / g1) ? FwdShape{g2, 2, whole} : plain;
+}
+
+// Per device and head dimension: the kernel's shared-memory opt-in, whether
+// its register split fits the launch, and how many clusters of two can be
+// resident at once.
+struct FwdDevInfo {
+  cudaError_t err;
+  bool regs_ok;
+  int max2;
+};
+
+template <int HD>
+const FwdDevInfo* fwd_dev_info(int dev) {
+  using C = fa::FwdCfg<HD>;
+  static std::once_flag once[64];
+  static FwdDevInfo info[64];
+  if (dev < 0 || dev >= 64) return nullptr;
+  std::call_once(once[dev], [&] {
+    FwdDevInfo& fi = info[dev];
+    fi = FwdDevInfo{cudaSuccess, false, 0};
+    fi.err = cudaFuncSetAttribute(fa::fa_fwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    // The warpgroups' register split draws on the registers the block is
+    // launched with; a split larger than that would never complete, so the
+    // kernel is not launched unless the built register count covers it.
+    cudaFuncAttributes fattr;
+    if (fi.err == cudaSuccess) fi.err = cudaFuncGetAttributes(&fattr, fa::fa_fwd_kernel<HD>);
+    fi.regs_ok = fi.err == cudaSuccess && 8 * C::kRegsSoftmax + 4 * C::kRegsControl <= 12 * fattr.numRegs;
+    if (fi.err == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2u);
+      cfg.blockDim = dim3(C::kThreads);
+      cfg.dynamicSmemBytes = C::kSmemBytes;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      // A failed query only disables the shared units.
+      if (cudaOccupancyMaxActiveClusters(&n, fa::fa_fwd_kernel<HD>, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+      }
+      fi.max2 = std::max(0, n);
+    }
+  });
+  return &info[dev];
+}
+
 // Units [0, whole_units) of a problem of total_units units run whole; the rest
 // (the last, partial round) are shared by CTA pairs. A launch covering only
 // part of the problem (unit_offset onwards, e.g. one head group of
@@ -108,23 +181,10 @@ fa_status_t launch(const void* Q, const void* K, const void* V, void* O, float* 
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
   // The dynamic shared-memory opt-in is per function and device context.
-  static std::once_flag attr_once[64];
-  static cudaError_t attr_err[64];
-  if (dev < 0 || dev >= 64) return FA_ERR_UNSUPPORTED;
-  static bool regs_ok[64];
-  std::call_once(attr_once[dev], [&] {
-    attr_err[dev] = cudaFuncSetAttribute(fa::fa_fwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
-    // The warpgroups' register split draws on the registers the block is
-    // launched with; a split larger than that would never complete, so the
-    // kernel is not launched unless the built register count covers it.
-    cudaFuncAttributes fattr;
-    if (attr_err[dev] == cudaSuccess) attr_err[dev] = cudaFuncGetAttributes(&fattr, fa::fa_fwd_kernel<HD>);
-    regs_ok[dev] = attr_err[dev] == cudaSuccess &&
-                   8 * C::kRegsSoftmax + 4 * C::kRegsControl <= 12 * fattr.numRegs;
-  });
-  if (attr_err[dev] != cudaSuccess) return cuda_fail(attr_err[dev]);
-  if (!regs_ok[dev]) return FA_ERR_UNSUPPORTED;
+  const FwdDevInfo* fi = fwd_dev_info<HD>(dev);
+  if (!fi) return FA_ERR_UNSUPPORTED;
+  if (fi->err != cudaSuccess) return cuda_fail(fi->err);
+  if (!fi->regs_ok) return FA_ERR_UNSUPPORTED;
 
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, Q, B * H, N, HD) || !make_map(&mk, K, B * H_kv, N_kv, HD) ||
@@ -149,29 +209,19 @@ fa_status_t launch(const void* Q, const void* K, const void* V, void* O, float* 
 
   // Persistent grid: one CTA per SM (the kernel's shared memory and tensor
   // memory allow no second), each walking units blockIdx.x + k * gridDim.x.
-  // When the units left after the whole rounds would occupy at most half of
-  // an even grid, the grid is launched as clusters of two CTAs and each pair
-  // shares one of those units, half of its key blocks each: the last round
-  // then takes about half as long.
-  const int sms = sm_count(dev);
-  int grid = std::min(p.num_units, sms);
+  const FwdShape sh = fwd_shape(plan ? plan->total_units : p.num_units, p.n_kv_blocks, sm_count(dev), fi->max2);
+  int grid = std::min(p.num_units, sh.grid);
   p.num_whole = p.num_units;
   p.split_tail = 0;
-  const int even = sms & ~1;
-  const int total = plan ? plan->total_units : p.num_units;
-  const int offset = plan ? plan->unit_offset : 0;
-  if (p.n_kv_blocks >= 4 && even >= 2) {   // at least two key blocks for each half
-    const int whole = total / even;
-    const int tail = total - whole * even;
-    if (tail > 0 && 2 * tail <= even) {
-      // This launch's units past the problem's whole rounds are shared; they
-      // are a suffix of its units and at most half the grid.
-      const int local_whole = std::max(0, std::min(p.num_units, whole * even - offset));
-      if (local_whole < p.num_units) {
-        p.split_tail = 1;
-        p.num_whole = local_whole;
-        grid = even;
-      }
+  if (sh.cluster == 2) {
+    // This launch's units past the problem's whole rounds are shared; they
+    // are a suffix of its units and at most half the grid.
+    const int offset = plan ? plan->unit_offset : 0;
+    const int local_whole = std::max(0, std::min(p.num_units, sh.whole_units - offset));
+    if (local_whole < p.num_units) {
+      p.split_tail = 1;
+      p.num_whole = local_whole;
+      grid = sh.grid;
     }
   }
   if (p.split_tail) {
@@ -559,6 +609,27 @@ extern "C" {
 fa_status_t fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
                    float scale, cudaStream_t stream) {
   return fwd_impl(Q, K, V, O, LSE, B, H, N, d, scale, -1, kDefaultTimeoutNs, stream);
+}
+
+fa_status_t fa_fwd_launch_shape(int B, int H, int N, int d, int* grid, int* cluster, int* whole_units) {
+  if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+  if (B > 65535 || H > 65535) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H * N >= (1LL << 31)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  int dev = 0;
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const FwdDevInfo* fi = d == 64 ? fwd_dev_info<64>(dev) : fwd_dev_info<128>(dev);
+  if (!fi) return FA_ERR_UNSUPPORTED;
+  if (fi->err != cudaSuccess) return cuda_fail(fi->err);
+  using C = fa::FwdCfg<128>;   // the unit and key-block sizes do not depend on d
+  const int unit_rows = C::kQTiles * C::kBM;
+  const int units = B * H * ((N + unit_rows - 1) / unit_rows);
+  const FwdShape sh = fwd_shape(units, (N + C::kBN - 1) / C::kBN, sm_count(dev), fi->max2);
+  if (grid) *grid = sh.grid;
+  if (cluster) *cluster = sh.cluster;
+  if (whole_units) *whole_units = sh.whole_units;
+  return FA_OK;
 }
 
 size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d) {

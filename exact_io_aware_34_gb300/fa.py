@@ -28,7 +28,7 @@ EXPORTED = ("fa_fwd", "fa_get_device_status", "fa_status_string", "fa_last_cuda_
             "fa_naive_fwd", "fa_naive_workspace_bytes", "fa_naive_fwd_noalloc", "fa_bwd", "fa_bwd_workspace_bytes",
             "fa_bwd_fault_test", "fa_fwd_kv", "fa_fwd_kv_num_splits", "fa_fwd_kv_workspace_bytes",
             "fa_fwd_kv_fault_test", "fa_merge_partials", "fa_fwd_host", "fa_fwd_host_workspace_bytes",
-            "fa_fwd_kv_f32", "fa_fwd_kv_f32_workspace_bytes")
+            "fa_fwd_kv_f32", "fa_fwd_kv_f32_workspace_bytes", "fa_fwd_launch_shape")
 
 _lib = None
 
@@ -90,6 +90,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_fwd_kv_f32.restype = i
     lib.fa_fwd_kv_f32_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
     lib.fa_fwd_kv_f32_workspace_bytes.restype = ctypes.c_size_t
+    ip = ctypes.POINTER(ctypes.c_int)
+    lib.fa_fwd_launch_shape.argtypes = [i, i, i, i, ip, ip, ip]
+    lib.fa_fwd_launch_shape.restype = i
     lib.fa_merge_partials.argtypes = [vp, vp, vp, vp, i, ctypes.c_longlong, i, vp]
     lib.fa_merge_partials.restype = i
     _lib = lib
@@ -236,6 +239,18 @@ def fa_naive_fwd(q, k, v, o=None, lse=None, scale: float | None = None, workspac
     if st != FA_OK:
         raise FaError(st, "fa_naive_fwd")
     return o, lse
+
+
+def fa_fwd_launch_shape(B: int, H: int, N: int, d: int) -> tuple:
+    """(grid, cluster, whole_units) of the launch fa_fwd makes for these sizes
+    on the current device: cluster is 1, or 2 when CTA pairs share the units
+    of the last, partial round."""
+    grid, cluster, whole = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    st = load_library().fa_fwd_launch_shape(int(B), int(H), int(N), int(d), ctypes.byref(grid),
+                                            ctypes.byref(cluster), ctypes.byref(whole))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_launch_shape")
+    return grid.value, cluster.value, whole.value
 
 
 def fa_fwd_kv_num_splits(B: int, H: int, H_kv: int, N_q: int, N_kv: int, d: int) -> int:

@@ -71,14 +71,30 @@ typedef enum {
  * The launch is a persistent grid of at most one CTA per SM walking units of
  * 256 query rows; when the units of its last, partial round fill at most
  * half of the SMs, it is launched as clusters of two CTAs that share those
- * units (half of the key blocks each, merged on chip). The result does not
- * depend on the stream or on other work on the GPU, but it does depend on
- * the SM count (which units are shared), like any reduction order.
+ * units (half of the key blocks each, merged on chip; see
+ * fa_fwd_launch_shape). The result does not depend on the stream or on other
+ * work on the GPU, but it does depend on the SM count (which units are
+ * shared), like any reduction order.
  * Follows: "Flash Attention (FA1)" tiling and online-softmax update;
  * "01 · 注意力为什么是 IO 瓶颈" §4/§6 for the O + LSE outputs.
  */
 fa_status_t fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
                    int B, int H, int N, int d, float scale, cudaStream_t stream);
+
+/*
+ * fa_fwd_launch_shape -- the launch fa_fwd makes for these sizes on the
+ * current device (informational; it launches nothing and reads no data).
+ *   grid        : host, receives the number of CTAs (at most the SM count).
+ *   cluster     : host, receives 1 (no shared units) or 2 (CTA pairs share
+ *                 the units of the last, partial round).
+ *   whole_units : host, receives how many units of 256 query rows are run
+ *                 whole by one CTA; the other B*H*ceil(N/256) - whole_units
+ *                 are shared.
+ * Any of the three may be NULL. Returns FA_ERR_INVALID_ARG or
+ * FA_ERR_UNSUPPORTED for sizes fa_fwd rejects, FA_ERR_CUDA if the device
+ * cannot be queried, else FA_OK.
+ */
+fa_status_t fa_fwd_launch_shape(int B, int H, int N, int d, int* grid, int* cluster, int* whole_units);
 
 /*
  * fa_fwd_host_workspace_bytes -- device workspace fa_fwd_host needs: room for

@@ -195,6 +195,21 @@ def kv_call(lib, **kw):
                          args["ws_bytes"], None)
 
 
+@pytest.mark.parametrize("sizes,expect", [
+    ((0, 1, 128, 128), fa.FA_ERR_INVALID_ARG),
+    ((1, 0, 128, 128), fa.FA_ERR_INVALID_ARG),
+    ((1, 1, 0, 128), fa.FA_ERR_INVALID_ARG),
+    ((65536, 1, 128, 128), fa.FA_ERR_INVALID_ARG),
+    ((1024, 1024, 2048, 128), fa.FA_ERR_INVALID_ARG),   # B*H*N >= 2^31
+    ((1, 1, 128, 96), fa.FA_ERR_UNSUPPORTED),
+])
+def test_launch_shape_rejects_sizes(lib, sizes, expect):
+    """The shape query checks sizes as fa_fwd does, before asking the device."""
+    with pytest.raises(fa.FaError) as e:
+        fa.fa_fwd_launch_shape(*sizes)
+    assert e.value.status == expect
+
+
 def test_kv_workspace_and_splits(lib):
     # 4 splits of 8 query rows (H = 8, N_q = 1) with d = 128: 4 * 8 * 129 floats
     assert fa.fa_fwd_kv_workspace_bytes(1, 8, 2, 1, 4096, 128, 4) == 4 * 8 * 129 * 4

@@ -31,6 +31,7 @@ def test_bench_line_has_the_contract_keys():
     assert d["value"] > 0 and d["gpu_launches"] == 3
     r = d["roofline"]
     assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and 0 < r["frac"] == pytest.approx(r["achieved"] / r["peak"])
+    assert r["launch"]["cluster"] in (1, 2) and 1 <= r["launch"]["grid"] <= 1024
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] == 3 * 32 * 8192 * 128 * 2
     assert e["d2h_bytes_per_step"] == 32 * 8192 * (128 * 2 + 4)

@@ -236,6 +236,23 @@ def test_whole_rounds_then_split_tail(d):
     print(d, err)
 
 
+def test_launch_shapes_of_the_workloads():
+    """The launch the benchmark workloads get on a 152-SM GB300: the 4096-row
+    shape (512 units) and the spiky 32k shape (2048 units) share their last
+    round in CTA pairs; the 8k prefill (1024 units, 112 left over) and the
+    1024-row d = 64 shape (256 units, 104 left over) run every unit whole,
+    since their leftovers are more than half the grid; the 256-row shape
+    runs 16 units; 40 heads of 1024 rows (160 units) share 8."""
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("the expected shapes are those of a 152-SM device")
+    assert fa.fa_fwd_launch_shape(2, 16, 4096, 128) == (152, 2, 456)
+    assert fa.fa_fwd_launch_shape(1, 16, 32768, 128) == (152, 2, 1976)
+    assert fa.fa_fwd_launch_shape(1, 32, 8192, 128) == (152, 1, 1024)
+    assert fa.fa_fwd_launch_shape(4, 16, 1024, 64) == (152, 1, 256)
+    assert fa.fa_fwd_launch_shape(1, 16, 256, 64) == (16, 1, 16)
+    assert fa.fa_fwd_launch_shape(1, 40, 1024, 128) == (152, 2, 152)
+
+
 def test_split_units_with_ragged_keys_and_negative_scale():
     """Split units where the second half ends in a ragged key block, with a
     negative scale (the scores negated on the tensor core)."""
