@@ -8,7 +8,7 @@ query row). The default workload is the 8k-context prefill shape
 TFLOP/s counted as 4*B*H*N^2*d / time. Rank 0 prints one JSON line.
 
 Timing: W untimed warm-up steps; then K steps, each bracketed by CUDA events
-on the launching stream, with the L2 cache flushed (a 512 MB write, then a 256 MB read) before
+on the launching stream, with the L2 cache flushed (a 512 MB write) before
 every step, outside the events; barrier + synchronize around the timed
 region; the max over ranks of the summed device time. For N > 1 (launched by
 torchrun; ``--gpus N`` without a torchrun environment starts N ranks itself)
@@ -496,23 +496,6 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------------------- native arm
-class L2Flush:
-    """Evicts the inputs from L2 before a timed step: a 512 MB write (four times the
-    129 MB L2), then a 256 MB read of another buffer, so that the written lines are
-    written back to DRAM here, outside the timed events, and not by the timed
-    kernel's own misses."""
-
-    def __init__(self, device):
-        import torch
-        self.buf = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
-        self.clean = torch.ones(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
-        self.sink = torch.zeros((), dtype=torch.float32, device=device)
-
-    def __call__(self, i):
-        self.buf.fill_(float(i))
-        self.sink.add_(self.clean.sum())
-
-
 def launch_shape(fa, shape):
     """The forward's launch for a [B, H, N, d] problem on this device: CTAs,
     CTAs per cluster (1, or 2 when pairs share the last round's units) and
@@ -532,7 +515,7 @@ def time_forward(fa, qd, kd, vd, o, lse, scale, flush, stream, steps, warmup, lo
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     with ClockSampler(local, uuid) as clocks:
         for i in range(steps):
-            flush(i)
+            flush.fill_(float(i))
             starts[i].record(stream)
             fa.fa_fwd(qd, kd, vd, o, lse, scale)
             ends[i].record(stream)
@@ -587,7 +570,7 @@ def run_native(args):
     qd, kd, vd = (x.to(device) for x in (q, k, v))
     o = torch.empty_like(qd)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
-    flush = L2Flush(device)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
 
     for _ in range(args.warmup):
@@ -608,7 +591,7 @@ def run_native(args):
         pass
     with ClockSampler(local, uuid) as clocks:
         for i in range(args.steps):
-            flush(i)
+            flush.fill_(float(i))
             starts[i].record(stream)
             fa.fa_fwd(qd, kd, vd, o, lse, scale)
             ends[i].record(stream)
@@ -650,7 +633,7 @@ def run_native(args):
                              "flops_per_launch": cw.flops,
                              "algorithmic_bytes_per_launch": cw.B * cw.H * cw.N * (8 * cw.d + 4)},
                 "gpu_launches": n_steps,
-                "l2": "flushed before every step (512 MB write, then a 256 MB read that leaves no dirty line; outside the events)",
+                "l2": "flushed before every step (512 MB write, outside the events)",
                 "clocks": c_clk,
             }
             if cw.name in cpu_cfg:
@@ -674,7 +657,7 @@ def run_native(args):
         cs = [torch.cuda.Event(enable_timing=True) for _ in range(n_steps)]
         ce = [torch.cuda.Event(enable_timing=True) for _ in range(n_steps)]
         for i in range(n_steps):
-            flush(i)
+            flush.fill_(float(i))
             cs[i].record(stream)
             fa.fa_naive_fwd(qd, kd, vd, o_n, lse_n, scale, ws)
             ce[i].record(stream)
@@ -713,7 +696,7 @@ def run_native(args):
         be = [torch.cuda.Event(enable_timing=True) for _ in range(n_steps)]
         with ClockSampler(local, uuid) as bclocks:
             for i in range(n_steps):
-                flush(i)
+                flush.fill_(float(i))
                 bs[i].record(stream)
                 fa.fa_bwd(qd, kd, vd, o, do, lse, dq, dk, dv, scale, ws_b)
                 be[i].record(stream)
@@ -759,7 +742,7 @@ def run_native(args):
         ee = [torch.cuda.Event(enable_timing=True) for _ in range(n_steps)]
         with ClockSampler(local, uuid) as dclocks:
             for i in range(n_steps):
-                flush(i)
+                flush.fill_(float(i))
                 es[i].record(stream)
                 fa.fa_fwd_kv(dq_, dk_, dv_, do_, dl_, dw.scale, 0, dws)
                 ee[i].record(stream)
@@ -816,7 +799,7 @@ def run_native(args):
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "strong" if args.shard == "heads" else "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded; Q,K ~ N(0,1), V ~ U(-1,1), bf16)",
-            "config": {**w.describe(), "l2": "flushed before every step (512 MB write, then a 256 MB read that leaves no dirty line; outside the events)",
+            "config": {**w.describe(), "l2": "flushed before every step (512 MB write, outside the events)",
                        "parallelism": (f"heads split over {world} ranks (no collective)" if args.shard == "heads"
                                        else f"replicas x{world} (independent problems per rank)")},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": UNIT,
