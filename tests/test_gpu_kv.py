@@ -130,6 +130,15 @@ def test_decode_workload_full():
     print(w.name, fa.fa_fwd_kv_num_splits(w.B, w.H, w.H_kv, w.N_q, w.N_kv, w.d), err)
 
 
+def test_decode_million_keys():
+    """One query row per head against 1,000,003 keys (7813 key blocks, the
+    last ragged) with 4 query heads on one K/V head: every output row against
+    the oracle (the key split merges ranges of about 900 blocks)."""
+    q, k, v = inputs.make_kv(1, 4, 1, 1, 1_000_003, 128, seed=390)
+    err, _, _ = check_kv(q, k, v, 1 / math.sqrt(128), two_x_rule=False)
+    print(fa.fa_fwd_kv_num_splits(1, 4, 1, 1, 1_000_003, 128), err)
+
+
 # --- failure path and rejections ---------------------------------------------------
 @pytest.mark.parametrize("N_q", [2, 300])
 @pytest.mark.parametrize("drop", [0, 1, 4])

@@ -236,6 +236,16 @@ def test_whole_rounds_then_split_tail(d):
     print(d, err)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_long_sequence_sampled_rows(d):
+    """131000 rows and keys per head (1024 key blocks per unit, the last one
+    ragged; 512 units of which the last is partial): sampled rows against the
+    oracle, every row finite and inside the range of V."""
+    q, k, v = inputs.make_random(1, 2, 131000, d, seed=80 + d)
+    err = parity.check_sampled(q, k, v, 1 / math.sqrt(d), n_rows=96, seed=d)
+    print(d, err)
+
+
 def test_launch_shapes_of_the_workloads():
     """The launch the benchmark workloads get on a 152-SM GB300: the 4096-row
     shape (512 units) and the spiky 32k shape (2048 units) share their last
