@@ -667,12 +667,21 @@ def run_native(args):
             raise RuntimeError(f"device status after the comparator: {fa.fa_status_string(st)} {info}")
         naive_ms = sum(a.elapsed_time(b) for a, b in zip(cs, ce)) / n_steps
         fused_ms = sum(step_ms) / len(step_ms)
+        # Its floor is HBM traffic: S written, read, written back as P and read
+        # by the PV product (4 x 2 bytes per score), plus Q, K, V read, O and
+        # LSE written.
+        n_bytes = 4 * 2 * B * H * N * N + 4 * 2 * B * H * N * d + 4 * B * H * N
+        peaks_c, peak_src_c = load_peaks()
         comparator = {
             "impl": "standard attention: S = QK^T, P = softmax(S) and O = PV as 3 launches, S/P in HBM (bf16)",
             "steps": n_steps, "ms_per_step": naive_ms, "value": flops / (naive_ms * 1e-3) / 1e12, "unit": UNIT,
             "speedup_of_fused": naive_ms / fused_ms,
             "workspace_bytes": ws_bytes, "fused_workspace_bytes": 0,
             "max_abs_diff_O_vs_fused": float((o_n.float() - o.float()).abs().max()),
+            "roofline": {"bound": "hbm", "achieved": n_bytes / (naive_ms * 1e-3) / 1e9, "peak": peaks_c["hbm_gbs"],
+                         "unit": "GB/s", "frac": n_bytes / (naive_ms * 1e-3) / 1e9 / peaks_c["hbm_gbs"],
+                         "algorithmic_bytes_per_call": n_bytes, "peak_source": f"{peak_src_c} HBM copy bandwidth",
+                         "kernels": "gemm_bf16_kernel<128, 1> (S), softmax_rows_kernel, gemm_bf16_kernel<d, 0> (PV)"},
         }
         del ws, o_n, lse_n
         torch.cuda.empty_cache()
