@@ -305,9 +305,9 @@ fa_status_t naive_launch(const void* Q, const void* K, const void* V, void* O, f
   static std::once_flag once[64];
   static cudaError_t attr_err[64];
   std::call_once(once[dev], [&] {
-    attr_err[dev] = gemm_attr<128, true>();
+    attr_err[dev] = cudaFuncSetAttribute(fa::naive::s_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         fa::naive::SGemmCfg::kSmemBytes);
     if (attr_err[dev] == cudaSuccess) attr_err[dev] = gemm_attr<HD, false>();
-
   });
   if (attr_err[dev] != cudaSuccess) return cuda_fail(attr_err[dev]);
 
@@ -320,11 +320,21 @@ fa_status_t naive_launch(const void* Q, const void* K, const void* V, void* O, f
     return cuda_fail(cudaErrorInvalidValue);
   auto* S = static_cast<__nv_bfloat16*>(ws);
 
-  // 1. S = bf16(scale * bf16(Q K^T))
-  fa::naive::GemmParams g1{S, N, N, HD, static_cast<int>(ld), scale, kNaiveTimeoutNs};
-  using G1 = fa::naive::GemmCfg<128, true>;
-  fa::naive::gemm_bf16_kernel<128, true><<<dim3((N + 127) / 128, (N + 127) / 128, BH), G1::kThreads, G1::kSmemBytes,
-                                           stream>>>(mq, mk, ms_out, g1);
+  // 1. S = bf16(scale * bf16(Q K^T)): a persistent grid of two CTAs per SM
+  using G1 = fa::naive::SGemmCfg;
+  fa::naive::SGemmParams g1;
+  g1.M = N;
+  g1.Nc = N;
+  g1.K = HD;
+  g1.mt = (N + G1::kBM - 1) / G1::kBM;
+  g1.nt = (N + G1::kBN - 1) / G1::kBN;
+  const long long s_tiles = static_cast<long long>(g1.mt) * g1.nt * BH;
+  if (s_tiles >= (1LL << 31)) return FA_ERR_UNSUPPORTED;
+  g1.tiles = static_cast<int>(s_tiles);
+  g1.alpha = scale;
+  g1.timeout_ns = kNaiveTimeoutNs;
+  const int s_grid = static_cast<int>(std::min<long long>(s_tiles, 2LL * sm_count(dev)));
+  fa::naive::s_gemm_kernel<<<s_grid, G1::kThreads, G1::kSmemBytes, stream>>>(mq, mk, ms_out, g1);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   // 2. P = softmax(S) row by row, in place; LSE = m + ln l
