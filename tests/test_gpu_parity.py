@@ -246,6 +246,36 @@ def test_long_sequence_sampled_rows(d):
     print(d, err)
 
 
+def _sweep_shapes():
+    """24 seeded shapes: odd lengths, both head sizes, both signs of scale, and
+    half of them with a unit count (B*H*ceil(N/256)) whose leftover after the
+    whole rounds on 152 SMs is 1-76 units, so that CTA pairs share the last
+    round (with 4 or more key blocks)."""
+    rng = np.random.default_rng(2024)
+    shapes = []
+    while len(shapes) < 24:
+        d = int(rng.choice([64, 128]))
+        scale = float(rng.uniform(0.02, 0.2) * rng.choice([-1, 1]))
+        if len(shapes) % 2 == 0:
+            N = int(rng.integers(1, 3000))
+            B, H = int(rng.integers(1, 4)), int(rng.integers(1, 24))
+        else:
+            N = int(rng.integers(513, 2600))            # 3-11 units per head, >= 5 key blocks
+            qb = (N + 255) // 256
+            target = 152 * int(rng.integers(1, 3)) + int(rng.integers(1, 77))
+            H = max(1, target // qb)
+            B = 1
+        shapes.append((B, H, N, d, scale))
+    return shapes
+
+
+@pytest.mark.parametrize("B,H,N,d,scale", _sweep_shapes())
+def test_seeded_shape_sweep(B, H, N, d, scale):
+    q, k, v = inputs.make_random(B, H, N, d, seed=B * 7919 + H * 104729 + N * 13 + d)
+    err = parity.check_sampled(q, k, v, scale, n_rows=48, seed=N, two_x_rule=N >= 64)
+    print(B, H, N, d, scale, fa.fa_fwd_launch_shape(B, H, N, d), err["o_max"], err["lse_max"])
+
+
 def test_launch_shapes_of_the_workloads():
     """The launch the benchmark workloads get on a 152-SM GB300: the 4096-row
     shape (512 units) and the spiky 32k shape (2048 units) share their last
