@@ -29,11 +29,16 @@
 // plus two 128-column score regions.
 //
 // The two score regions R0, R1 alternate: block i's S goes to R[i&1] and its
-// dP to R[(i+1)&1]. Once the softmax warps have loaded both, the MMA warp
-// issues block i+1's S into R[(i+1)&1] while the softmax warps compute; they
-// write the packed bf16 results (P and dS, or dS alone) over S_i in R[i&1].
-// The tile products of block i that read those results, then block i+1's dP
+// dP to R[(i+1)&1]. S and dP complete on barriers of their own, so that the
+// elementwise warps take the exponentials of block i as soon as its S is
+// done, while the tensor core still works on block i-1's gradient products
+// and block i's dP; only dS = P (dP - D) is left for after dP. Once they have
+// loaded dP_i, the MMA warp issues block i+1's S into R[(i+1)&1]; they write
+// the packed bf16 results (P and dS, or dS alone) over S_i in R[i&1]. The
+// tile products of block i that read those results, then block i+1's dP
 // (into R[i&1]), follow in issue order, which the tensor core keeps.
+// (In the query-block kernel, with S and dP in regions of their own, S_{j+1}
+// goes in as soon as S_j has been loaded, and dP_{j+1} once dP_j has.)
 //
 // In the key-block kernel Q_i and dO_i share a ring slot but each has its own
 // full and empty barriers. dK (the last reader of Q_i) is issued before dV
@@ -243,7 +248,9 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tmQ, const CUtenso
   __shared__ __align__(8) uint64_t bar_k_empty[D::kKSlots];
   __shared__ __align__(8) uint64_t bar_v_full[D::kVSlots];
   __shared__ __align__(8) uint64_t bar_v_empty[D::kVSlots];
-  __shared__ __align__(8) uint64_t bar_s_full;
+  __shared__ __align__(8) uint64_t bar_st_full;    // S_j complete
+  __shared__ __align__(8) uint64_t bar_dpt_full;   // dP_j complete
+  __shared__ __align__(8) uint64_t bar_s_free;     // S_j loaded (and K_{j+1} landed)
   __shared__ __align__(8) uint64_t bar_dp_free;
   __shared__ __align__(8) uint64_t bar_p_full[2];
   __shared__ __align__(8) uint64_t bar_acc_full;
@@ -272,7 +279,9 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tmQ, const CUtenso
       ptx::mbar_init(ptx::smem_u32(&bar_v_full[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&bar_v_empty[s]), 1);
     }
-    ptx::mbar_init(ptx::smem_u32(&bar_s_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&bar_st_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&bar_dpt_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&bar_s_free), 256);
     ptx::mbar_init(ptx::smem_u32(&bar_dp_free), 256);
     ptx::mbar_init(ptx::smem_u32(&bar_p_full[0]), 256);
     ptx::mbar_init(ptx::smem_u32(&bar_p_full[1]), 256);
@@ -352,29 +361,37 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tmQ, const CUtenso
     {
       auto k_tile = [&](int j) { return sK + (j % D::kKSlots) * C::kTileBytes; };
       auto v_tile = [&](int j) { return sV + (j % D::kVSlots) * C::kTileBytes; };
-      // S_j = Q K_j^T and dP_j = dO V_j^T. K_0 and V_0 are waited for here;
-      // every later K_{j+1} and V_{j+1} by the elementwise warps before their
+      // S_j = Q K_j^T and dP_j = dO V_j^T, each committed to its own barrier.
+      // K_0 and V_0 are waited for here; every later K_{j+1} by the
+      // elementwise warps before their s_free(j), and V_{j+1} before their
       // dp_free(j), so that this warp waits only on the hand-offs.
-      auto issue_sdp = [&](int j) -> bool {
-        if (j == 0) {
-          if (!wait_warp_or_abort(ptx::smem_u32(&bar_k_full[0]), 0, abort_ptr, p.timeout_ns, kRoleDqMma)) return false;
-          if (!wait_warp_or_abort(ptx::smem_u32(&bar_v_full[0]), 0, abort_ptr, p.timeout_ns, kRoleDqMma)) return false;
-        }
+      auto issue_s = [&](int j) {
         ptx::tc_fence_after();
         issue_tile_qk<HD>(tmem_base + D::kColS, sQ, k_tile(j));
+        ptx::mma_commit_warp(ptx::smem_u32(&bar_st_full));
+      };
+      auto issue_dp = [&](int j) {
+        ptx::tc_fence_after();
         issue_tile_qk<HD>(tmem_base + D::kColP, sdO, v_tile(j));
         ptx::mma_commit_warp(ptx::smem_u32(&bar_v_empty[j % D::kVSlots]));
-        ptx::mma_commit_warp(ptx::smem_u32(&bar_s_full));
-        return true;
+        ptx::mma_commit_warp(ptx::smem_u32(&bar_dpt_full));
       };
       bool ok = wait_warp_or_abort(ptx::smem_u32(&bar_in_full), 0, abort_ptr, p.timeout_ns, kRoleDqMma);
-      if (ok) ok = issue_sdp(0);
+      if (ok) ok = wait_warp_or_abort(ptx::smem_u32(&bar_k_full[0]), 0, abort_ptr, p.timeout_ns, kRoleDqMma);
+      if (ok) ok = wait_warp_or_abort(ptx::smem_u32(&bar_v_full[0]), 0, abort_ptr, p.timeout_ns, kRoleDqMma);
+      if (ok) {
+        issue_s(0);
+        issue_dp(0);
+      }
       for (int j = 0; j < n && ok; ++j) {
         if (j + 1 < n) {
+          // S_{j+1} as soon as S_j has been read; dP_{j+1} once dP_j has.
+          ok = wait_warp_or_abort(ptx::smem_u32(&bar_s_free), j & 1, abort_ptr, p.timeout_ns, kRoleDqMma);
+          if (!ok) break;
+          issue_s(j + 1);
           ok = wait_warp_or_abort(ptx::smem_u32(&bar_dp_free), j & 1, abort_ptr, p.timeout_ns, kRoleDqMma);
           if (!ok) break;
-          ok = issue_sdp(j + 1);
-          if (!ok) break;
+          issue_dp(j + 1);
         }
         ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_full[j & 1]), (j >> 1) & 1, abort_ptr, p.timeout_ns, kRoleDqMma);
         if (!ok) break;
@@ -406,35 +423,27 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tmQ, const CUtenso
     const uint32_t tP = tmem_base + lane_addr + D::kColP + 64u * half;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
-      ok = wait_warp_or_abort(ptx::smem_u32(&bar_s_full), j & 1, abort_ptr, p.timeout_ns, kRoleDqSoftmax);
+      ok = wait_warp_or_abort(ptx::smem_u32(&bar_st_full), j & 1, abort_ptr, p.timeout_ns, kRoleDqSoftmax);
       if (!ok) break;
       ptx::tc_fence_after();
       uint32_t s[2][32], dp[2][32];
       ptx::tmem_ld32(tS, s[0]);
       ptx::tmem_ld32(tS + 32, s[1]);
-      ptx::tmem_ld32(tP, dp[0]);
-      ptx::tmem_ld32(tP + 32, dp[1]);
       ptx::tmem_ld_wait();
       ptx::reg_fence32(s[0]);
       ptx::reg_fence32(s[1]);
-      ptx::reg_fence32(dp[0]);
-      ptx::reg_fence32(dp[1]);
       if (j + 1 < n) {
-        // K_{j+1} and V_{j+1} in place before the hand-off that lets S/dP of
-        // block j+1 be issued.
+        // K_{j+1} in place before the hand-off that lets S_{j+1} be issued.
         ok = wait_warp_or_abort(ptx::smem_u32(&bar_k_full[(j + 1) % D::kKSlots]), ((j + 1) / D::kKSlots) & 1,
                                 abort_ptr, p.timeout_ns, kRoleDqSoftmax);
-        if (ok)
-          ok = wait_warp_or_abort(ptx::smem_u32(&bar_v_full[(j + 1) % D::kVSlots]), ((j + 1) / D::kVSlots) & 1,
-                                  abort_ptr, p.timeout_ns, kRoleDqSoftmax);
         if (!ok) break;
       }
       ptx::tc_fence_before();
-      ptx::mbar_arrive(ptx::smem_u32(&bar_dp_free));
+      ptx::mbar_arrive(ptx::smem_u32(&bar_s_free));
 
       const int valid = p.N - j * C::kBlk - 64 * half;   // keys of this warp's 64 that exist
       const bool ragged = valid < 64;
-      uint32_t pds[32];
+      // P (float32, kept in s) while dP_j is still on the tensor core.
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
 #pragma unroll
@@ -449,10 +458,36 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tmQ, const CUtenso
             if (32 * c + 2 * k >= valid) p0 = 0.f;
             if (32 * c + 2 * k + 1 >= valid) p1 = 0.f;
           }
+          s[c][2 * k] = __float_as_uint(p0);
+          s[c][2 * k + 1] = __float_as_uint(p1);
+        }
+      }
+      ok = wait_warp_or_abort(ptx::smem_u32(&bar_dpt_full), j & 1, abort_ptr, p.timeout_ns, kRoleDqSoftmax);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      ptx::tmem_ld32(tP, dp[0]);
+      ptx::tmem_ld32(tP + 32, dp[1]);
+      ptx::tmem_ld_wait();
+      ptx::reg_fence32(dp[0]);
+      ptx::reg_fence32(dp[1]);
+      if (j + 1 < n) {
+        // V_{j+1} in place before the hand-off that lets dP_{j+1} be issued.
+        ok = wait_warp_or_abort(ptx::smem_u32(&bar_v_full[(j + 1) % D::kVSlots]), ((j + 1) / D::kVSlots) & 1,
+                                abort_ptr, p.timeout_ns, kRoleDqSoftmax);
+        if (!ok) break;
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(ptx::smem_u32(&bar_dp_free));
+      uint32_t pds[32];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
           const uint64_t t =
               ptx::f2_add(ptx::f2_pack(__uint_as_float(dp[c][2 * k]), __uint_as_float(dp[c][2 * k + 1])), ndx2);
           float d0, d1;
-          ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(p0, p1), t), d0, d1);
+          ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(s[c][2 * k]), __uint_as_float(s[c][2 * k + 1])), t),
+                         d0, d1);
           pds[16 * c + k] = ptx::pack_bf16x2(d0, d1);
         }
       }
@@ -495,7 +530,8 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
   __shared__ __align__(8) uint64_t bar_q_empty[C::kStages];    // dK(i) done with Q_i
   __shared__ __align__(8) uint64_t bar_do_full[C::kStages];    // dO_i and -D landed
   __shared__ __align__(8) uint64_t bar_do_empty[C::kStages];   // dV(i) done with dO_i
-  __shared__ __align__(8) uint64_t bar_s_full;
+  __shared__ __align__(8) uint64_t bar_st_full;    // S^T(i) complete
+  __shared__ __align__(8) uint64_t bar_dpt_full;   // dP^T(i) complete
   __shared__ __align__(8) uint64_t bar_dp_free;
   __shared__ __align__(8) uint64_t bar_p_full;
   __shared__ __align__(8) uint64_t bar_acc_full;
@@ -524,7 +560,8 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
       ptx::mbar_init(ptx::smem_u32(&bar_do_full[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&bar_do_empty[s]), 1);
     }
-    ptx::mbar_init(ptx::smem_u32(&bar_s_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&bar_st_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&bar_dpt_full), 1);
     ptx::mbar_init(ptx::smem_u32(&bar_dp_free), 256);
     ptx::mbar_init(ptx::smem_u32(&bar_p_full), 256);
     ptx::mbar_init(ptx::smem_u32(&bar_acc_full), 1);
@@ -620,12 +657,13 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
       if (ok) {
         ptx::tc_fence_after();
         issue_tile_qk<HD>(region(0), sK, q_tile(0));                   // S_0^T = K Q_0^T
+        ptx::mma_commit_warp(ptx::smem_u32(&bar_st_full));
       }
       if (ok) ok = wait_warp_or_abort(ptx::smem_u32(&bar_do_full[0]), 0, abort_ptr, p.timeout_ns, kRoleDkvMma);
       if (ok) {
         ptx::tc_fence_after();
         issue_tile_qk<HD>(region(1), sV, q_tile(0) + C::kTileBytes);   // dP_0^T = V dO_0^T
-        ptx::mma_commit_warp(ptx::smem_u32(&bar_s_full));
+        ptx::mma_commit_warp(ptx::smem_u32(&bar_dpt_full));
       }
       for (int i = 0; i < n && ok; ++i) {
         // S_{i+1}^T goes in as soon as region(i+1) is free (dp_free(i)) and
@@ -644,6 +682,7 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
             if (__all_sync(0xffffffffu, ptx::mbar_test_wait(q_full1, in_par))) {
               ptx::tc_fence_after();
               issue_tile_qk<HD>(region(i + 1), sK, q_tile(i + 1));      // S_{i+1}^T
+              ptx::mma_commit_warp(ptx::smem_u32(&bar_st_full));
               s_issued = true;
               break;
             }
@@ -665,12 +704,13 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
             if (!ok) break;
             ptx::tc_fence_after();
             issue_tile_qk<HD>(region(i + 1), sK, q_tile(i + 1));        // S_{i+1}^T
+            ptx::mma_commit_warp(ptx::smem_u32(&bar_st_full));
           }
           ok = wait_warp_or_abort(ptx::smem_u32(&bar_do_full[s1]), in_par, abort_ptr, p.timeout_ns, kRoleDkvMma);
           if (!ok) break;
           ptx::tc_fence_after();
           issue_tile_qk<HD>(region(i), sV, q_tile(i + 1) + C::kTileBytes);   // dP_{i+1}^T
-          ptx::mma_commit_warp(ptx::smem_u32(&bar_s_full));
+          ptx::mma_commit_warp(ptx::smem_u32(&bar_dpt_full));
         }
       }
       if (ok) {
@@ -690,7 +730,9 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
     const uint64_t sl2x2 = ptx::f2_pack(p.scale_log2, p.scale_log2);
     bool ok = true;
     for (int i = 0; i < n; ++i) {
-      ok = wait_warp_or_abort(ptx::smem_u32(&bar_s_full), i & 1, abort_ptr, p.timeout_ns, kRoleDkvSoftmax);
+      // P^T as soon as S^T(i) is complete (it overlaps the tensor core's dK/dV
+      // of the previous block and dP^T of this one), then dS^T once dP^T(i) is.
+      ok = wait_warp_or_abort(ptx::smem_u32(&bar_st_full), i & 1, abort_ptr, p.timeout_ns, kRoleDkvSoftmax);
       if (!ok) break;
       ptx::tc_fence_after();
       const uint32_t tS = tmem_base + lane_addr + kColR + 128u * (i & 1) + 64u * half;
@@ -698,46 +740,65 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
       uint32_t s[2][32], dp[2][32];
       ptx::tmem_ld32(tS, s[0]);
       ptx::tmem_ld32(tS + 32, s[1]);
-      ptx::tmem_ld32(tP, dp[0]);
-      ptx::tmem_ld32(tP + 32, dp[1]);
       ptx::tmem_ld_wait();
       ptx::reg_fence32(s[0]);
       ptx::reg_fence32(s[1]);
+      // -LSE*log2e and -D of this warp's 64 query columns (broadcast reads).
+      const float4* vl = reinterpret_cast<const float4*>(vec + (i % C::kStages) * (C::kVecBytes / 4) + 64 * half);
+      const float4* vd = vl + 32;    // + 128 floats
+      {
+        uint32_t pp[32];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float4 l4 = vl[8 * c + u];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const int e = 4 * u + 2 * h2;
+              const uint64_t nl2 = h2 ? ptx::f2_pack(l4.z, l4.w) : ptx::f2_pack(l4.x, l4.y);
+              float x0, x1;
+              ptx::f2_unpack(
+                  ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1])), sl2x2, nl2), x0,
+                  x1);
+              const float p0 = ptx::ex2_approx(x0);
+              const float p1 = ptx::ex2_approx(x1);
+              s[c][e] = __float_as_uint(p0);
+              s[c][e + 1] = __float_as_uint(p1);
+              pp[16 * c + 2 * u + h2] = ptx::pack_bf16x2(p0, p1);
+            }
+          }
+        }
+        ptx::tmem_st32(tS, pp);
+        ptx::tmem_st_wait();
+      }
+      ok = wait_warp_or_abort(ptx::smem_u32(&bar_dpt_full), i & 1, abort_ptr, p.timeout_ns, kRoleDkvSoftmax);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      ptx::tmem_ld32(tP, dp[0]);
+      ptx::tmem_ld32(tP + 32, dp[1]);
+      ptx::tmem_ld_wait();
       ptx::reg_fence32(dp[0]);
       ptx::reg_fence32(dp[1]);
       ptx::tc_fence_before();
       ptx::mbar_arrive(ptx::smem_u32(&bar_dp_free));
-
-      // -LSE*log2e and -D of this warp's 64 query columns (broadcast reads).
-      const float4* vl = reinterpret_cast<const float4*>(vec + (i % C::kStages) * (C::kVecBytes / 4) + 64 * half);
-      const float4* vd = vl + 32;    // + 128 floats
-      uint32_t pp[32], pds[32];
+      uint32_t pds[32];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const float4 l4 = vl[8 * c + u];
           const float4 d4 = vd[8 * c + u];
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
-            const int e = 4 * u + 2 * h2;     // column within the 32-column piece
-            const uint64_t nl2 = h2 ? ptx::f2_pack(l4.z, l4.w) : ptx::f2_pack(l4.x, l4.y);
+            const int e = 4 * u + 2 * h2;
             const uint64_t nd2 = h2 ? ptx::f2_pack(d4.z, d4.w) : ptx::f2_pack(d4.x, d4.y);
-            float x0, x1;
-            ptx::f2_unpack(
-                ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1])), sl2x2, nl2), x0,
-                x1);
-            const float p0 = ptx::ex2_approx(x0);
-            const float p1 = ptx::ex2_approx(x1);
             const uint64_t t = ptx::f2_add(ptx::f2_pack(__uint_as_float(dp[c][e]), __uint_as_float(dp[c][e + 1])), nd2);
             float d0, d1;
-            ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(p0, p1), t), d0, d1);
-            pp[16 * c + 2 * u + h2] = ptx::pack_bf16x2(p0, p1);
+            ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(s[c][e]), __uint_as_float(s[c][e + 1])), t), d0, d1);
             pds[16 * c + 2 * u + h2] = ptx::pack_bf16x2(d0, d1);
           }
         }
       }
-      ptx::tmem_st32(tS, pp);
       ptx::tmem_st32(tS + 32, pds);
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
