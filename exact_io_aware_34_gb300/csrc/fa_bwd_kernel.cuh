@@ -41,10 +41,11 @@
 // goes in as soon as S_j has been loaded, and dP_{j+1} once dP_j has.)
 //
 // In the key-block kernel Q_i and dO_i share a ring slot but each has its own
-// full and empty barriers. dK (the last reader of Q_i) is issued before dV
-// (the last reader of dO_i), so the copy of Q into a freed slot starts one
-// tile product earlier than the copy of dO; S^T of the next block, which
-// needs Q alone, goes in as soon as its region is free and Q has landed.
+// full and empty barriers. dV_i needs only P_i^T and dO_i, so it is issued
+// right behind dP_i^T as soon as the elementwise warps have stored P_i^T, and
+// runs while they compute dS_i^T; dK_i follows their last hand-off. S^T of
+// the next block, which needs Q alone, goes in as soon as its region is free
+// and Q has landed.
 //
 // Warp roles (10 warps, as in the forward kernel):
 //   warps 0-7  elementwise step + epilogue: warp w serves TMEM lane quarter
@@ -534,6 +535,7 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
   __shared__ __align__(8) uint64_t bar_dpt_full;   // dP^T(i) complete
   __shared__ __align__(8) uint64_t bar_dp_free;
   __shared__ __align__(8) uint64_t bar_p_full;
+  __shared__ __align__(8) uint64_t bar_pt_stored;  // P^T(i) packed into TMEM
   __shared__ __align__(8) uint64_t bar_acc_full;
   __shared__ __align__(8) uint64_t bar_drain;
   __shared__ uint32_t tmem_base_slot;
@@ -564,6 +566,7 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
     ptx::mbar_init(ptx::smem_u32(&bar_dpt_full), 1);
     ptx::mbar_init(ptx::smem_u32(&bar_dp_free), 256);
     ptx::mbar_init(ptx::smem_u32(&bar_p_full), 256);
+    ptx::mbar_init(ptx::smem_u32(&bar_pt_stored), 256);
     ptx::mbar_init(ptx::smem_u32(&bar_acc_full), 1);
     ptx::mbar_init(ptx::smem_u32(&bar_drain), 1);
     abort_flag = 0;
@@ -664,6 +667,13 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
         ptx::tc_fence_after();
         issue_tile_qk<HD>(region(1), sV, q_tile(0) + C::kTileBytes);   // dP_0^T = V dO_0^T
         ptx::mma_commit_warp(ptx::smem_u32(&bar_dpt_full));
+        // dV_0 as soon as P_0^T is in place: it runs while dS_0^T is computed.
+        ok = wait_warp_or_abort(ptx::smem_u32(&bar_pt_stored), 0, abort_ptr, p.timeout_ns, kRoleDkvMma);
+        if (ok) {
+          ptx::tc_fence_after();
+          issue_tile_acc<HD, 64>(tmem_base + kColDV, region(0), q_tile(0) + C::kTileBytes, false);   // dV += P^T dO_0
+          ptx::mma_commit_warp(ptx::smem_u32(&bar_do_empty[0]));
+        }
       }
       for (int i = 0; i < n && ok; ++i) {
         // S_{i+1}^T goes in as soon as region(i+1) is free (dp_free(i)) and
@@ -696,8 +706,6 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
         ptx::tc_fence_after();
         issue_tile_acc<HD, 64>(tmem_base + kColDK, region(i) + 32, q_tile(i), i > 0);             // dK += dS^T Q_i
         ptx::mma_commit_warp(ptx::smem_u32(&bar_q_empty[i % C::kStages]));
-        issue_tile_acc<HD, 64>(tmem_base + kColDV, region(i), q_tile(i) + C::kTileBytes, i > 0);   // dV += P^T dO_i
-        ptx::mma_commit_warp(ptx::smem_u32(&bar_do_empty[i % C::kStages]));
         if (i + 1 < n) {
           if (!s_issued) {
             ok = wait_warp_or_abort(q_full1, in_par, abort_ptr, p.timeout_ns, kRoleDkvMma);
@@ -711,6 +719,12 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
           ptx::tc_fence_after();
           issue_tile_qk<HD>(region(i), sV, q_tile(i + 1) + C::kTileBytes);   // dP_{i+1}^T
           ptx::mma_commit_warp(ptx::smem_u32(&bar_dpt_full));
+          // dV_{i+1} right behind it once P_{i+1}^T is in place.
+          ok = wait_warp_or_abort(ptx::smem_u32(&bar_pt_stored), (i + 1) & 1, abort_ptr, p.timeout_ns, kRoleDkvMma);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          issue_tile_acc<HD, 64>(tmem_base + kColDV, region(i + 1), q_tile(i + 1) + C::kTileBytes, true);   // dV
+          ptx::mma_commit_warp(ptx::smem_u32(&bar_do_empty[(i + 1) % C::kStages]));
         }
       }
       if (ok) {
@@ -771,6 +785,8 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
         }
         ptx::tmem_st32(tS, pp);
         ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(ptx::smem_u32(&bar_pt_stored));
       }
       ok = wait_warp_or_abort(ptx::smem_u32(&bar_dpt_full), i & 1, abort_ptr, p.timeout_ns, kRoleDkvSoftmax);
       if (!ok) break;
