@@ -63,6 +63,11 @@
 // sub-partition); setmaxnreg then moves registers from the control
 // warpgroup (down to 72) to the softmax warpgroups (up to 216), which hold a
 // 128-score row plus its packed probabilities without spilling.
+// P is handed to the issuer in two halves: once the probabilities of keys
+// 0-63 are stored (and O_t rescaled, if it is), the issuer runs the first
+// four K = 16 products of P V while the softmax warps exponentiate keys
+// 64-127; the other four follow the second hand-off. Both halves sum in the
+// same order as one burst, so the result is unchanged.
 // TMEM (512 columns x 128 lanes x 32 bit): S_t at column 128*t (P_t, packed
 // bf16, overwrites the first 64 of those columns), O_t at 256 + d*t.
 // Shared memory: Q tiles (2 x 128 x d bf16) + a ring of K/V tiles
@@ -259,6 +264,7 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
   __shared__ __align__(8) uint64_t bar_kv_empty[C::kStages];
   __shared__ __align__(8) uint64_t bar_s_full[2];
   __shared__ __align__(8) uint64_t bar_p_full[2];
+  __shared__ __align__(8) uint64_t bar_p_half[2];   // P_t of keys 0-63 stored (and O_t rescaled)
   __shared__ __align__(8) uint64_t bar_o_full[2];
   __shared__ __align__(8) uint64_t bar_drain;
   // Split units: the partner CTA's producer arrives on bar_peer_ready when
@@ -298,6 +304,7 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
     for (int t = 0; t < 2; ++t) {
       ptx::mbar_init(ptx::smem_u32(&bar_s_full[t]), 1);
       ptx::mbar_init(ptx::smem_u32(&bar_p_full[t]), C::kBM);
+      ptx::mbar_init(ptx::smem_u32(&bar_p_half[t]), C::kBM);
       ptx::mbar_init(ptx::smem_u32(&bar_o_full[t]), 1);
     }
     ptx::mbar_init(ptx::smem_u32(&bar_drain), 1);
@@ -428,14 +435,17 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
     // compete for issue slots.
     // P V for query tile t from the V tile loaded as the it-th K/V load (P_t
     // sits in the S_t columns); the first product of a unit overwrites O_t.
-    auto issue_pv = [&](int t, int it, bool accumulate) {
+    auto issue_pv_half = [&](int t, int it, bool accumulate, int half) {
       const uint32_t v_tile = sKV + (it % C::kStages) * C::kTileBytes;
       const uint32_t d_tmem = tmem_base + C::kColO + HD * t;
       const uint32_t a_tmem = tmem_base + C::kColS + 128 * t;
-      static_assert(C::kBN == 128, "one burst of eight K = 16 products");
+      static_assert(C::kBN == 128, "two bursts of four K = 16 products");
       const uint64_t b_desc = ptx::desc_mnmajor_sw128(v_tile, C::kChunkBytes);
-      ptx::mma_ts_k128_warp<32>(d_tmem, a_tmem, ptx::desc_lo(b_desc), ptx::desc_hi(b_desc), C::kIdescPV,
-                                accumulate ? 1u : 0u);
+      if (half == 0)
+        ptx::mma_ts_k64half_warp<0>(d_tmem, a_tmem, ptx::desc_lo(b_desc), ptx::desc_hi(b_desc), C::kIdescPV,
+                                    accumulate ? 1u : 0u);
+      else
+        ptx::mma_ts_k64half_warp<1>(d_tmem, a_tmem, ptx::desc_lo(b_desc), ptx::desc_hi(b_desc), C::kIdescPV, 1u);
     };
     // S_t = Q_t K^T with the K tile of the it-th K/V load.
     auto issue_qk = [&](int t, int it) {
@@ -449,8 +459,9 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
         ptx::mma_ss_k64_warp(d_tmem, ptx::desc_lo(a_desc), ptx::desc_lo(b_desc), ptx::desc_hi(a_desc), p.idesc_qk, 0u);
     };
     // Per unit: Q and K_0 are waited for here; every later K_{j+1} and V_j
-    // is waited for by the softmax warps before their hand-off for block j
-    // (p_full), so the p_full waits below imply those tiles have landed. An
+    // is waited for by the softmax warps before their first hand-off for
+    // block j (p_half), so the p_half / p_full waits below imply those tiles
+    // have landed. An
     // mbarrier wait in this warp stalls the queued tensor-core work, so it
     // does as few as it can. g counts the key blocks of all units so far
     // (the phase of s_full / p_full).
@@ -467,10 +478,14 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
         ptx::tc_fence_after();
         for (int t = 0; t < 2 && ok; ++t) {
           if (j > 0) {
+            ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_half[t]), (g - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            issue_pv_half(t, itK - 1, j > 1, 0);
             ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_full[t]), (g - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
             if (!ok) break;
             ptx::tc_fence_after();
-            issue_pv(t, itK - 1, j > 1);
+            issue_pv_half(t, itK - 1, true, 1);
             if (t == 1) ptx::mma_commit_warp(ptx::smem_u32(&bar_kv_empty[(itK - 1) % C::kStages]));
           }
           issue_qk(t, itK);
@@ -485,10 +500,14 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
       // The last key block's P V.
       const int itV = it0 + 2 * n_kv - 1;
       for (int t = 0; t < 2 && ok; ++t) {
+        ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_half[t]), (g - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        issue_pv_half(t, itV, n_kv > 1, 0);
         ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_full[t]), (g - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
         if (!ok) break;
         ptx::tc_fence_after();
-        issue_pv(t, itV, n_kv > 1);
+        issue_pv_half(t, itV, true, 1);
         ptx::mma_commit_warp(ptx::smem_u32(&bar_o_full[t]));
         if (t == 1) ptx::mma_commit_warp(ptx::smem_u32(&bar_kv_empty[itV % C::kStages]));
       }
@@ -506,10 +525,14 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
         ptx::tc_fence_after();
         for (int t = 0; t < 2 && ok; ++t) {
           if (j > 0) {
+            ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_half[t]), (g - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            issue_pv_half(t, itK - 1, j > 1, 0);
             ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_full[t]), (g - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
             if (!ok) break;
             ptx::tc_fence_after();
-            issue_pv(t, itK - 1, j > 1);
+            issue_pv_half(t, itK - 1, true, 1);
             if (t == 1) ptx::mma_commit_warp(ptx::smem_u32(&bar_kv_empty[(itK - 1) % C::kStages]));
           }
           issue_qk(t, itK);
@@ -522,10 +545,14 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
       }
       const int itV = it0 + 2 * nb - 1;
       for (int t = 0; t < 2 && ok; ++t) {
+        ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_half[t]), (g - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        issue_pv_half(t, itV, nb > 1, 0);
         ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_full[t]), (g - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
         if (!ok) break;
         ptx::tc_fence_after();
-        issue_pv(t, itV, nb > 1);
+        issue_pv_half(t, itV, true, 1);
         ptx::mma_commit_warp(ptx::smem_u32(&bar_o_full[t]));
         if (t == 1) ptx::mma_commit_warp(ptx::smem_u32(&bar_kv_empty[itV % C::kStages]));
       }
@@ -627,7 +654,41 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
       uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
       uint32_t pk[2][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          float x0, x1;
+          ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[c][i]), __uint_as_float(s[c][i + 1])), sl2x2,
+                                     negmx2),
+                         x0, x1);
+          float p0 = ptx::ex2_approx(x0);
+          float p1 = ptx::ex2_approx(x1);
+          if (ragged) {   // exact zeros for keys past N (also when scale == 0)
+            if (32 * c + i >= valid) p0 = 0.f;
+            if (32 * c + i + 1 >= valid) p1 = 0.f;
+          }
+          acc[(i >> 1) & 3] = ptx::f2_add(acc[(i >> 1) & 3], ptx::f2_pack(p0, p1));
+          pk[c >> 1][(c & 1) * 16 + (i >> 1)] = ptx::pack_bf16x2(p0, p1);
+        }
+      }
+      if (rescale_o) {
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t o[32];
+          ptx::tmem_ld32(tO + 32 * c, o);
+          ptx::tmem_ld_wait();
+          ptx::reg_fence32(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          ptx::tmem_st32(tO + 32 * c, o);
+        }
+      }
+      ptx::tmem_st32(tS, pk[0]);
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(ptx::smem_u32(&bar_p_half[t]));
+#pragma unroll
+      for (int c = 2; c < 4; ++c) {
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
           float x0, x1;
@@ -659,20 +720,7 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
       const float pmax = ptx::ex2_approx(fmaf(mt, sl2, neg_m));
       l = l * alpha + sum;
       lo = lo * alpha + (sum + (ptx::round_bf16(pmax) - pmax));
-      ptx::tmem_st32(tS, pk[0]);
       ptx::tmem_st32(tS + 32, pk[1]);
-      if (rescale_o) {
-#pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
-          uint32_t o[32];
-          ptx::tmem_ld32(tO + 32 * c, o);
-          ptx::tmem_ld_wait();
-          ptx::reg_fence32(o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          ptx::tmem_st32(tO + 32 * c, o);
-        }
-      }
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       ptx::mbar_arrive(ptx::smem_u32(&bar_p_full[t]));
@@ -787,7 +835,41 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
         uint32_t pk[2][32];
   #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
+  #pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float x0, x1;
+            ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[c][i]), __uint_as_float(s[c][i + 1])), sl2x2,
+                                       negmx2),
+                           x0, x1);
+            float p0 = ptx::ex2_approx(x0);
+            float p1 = ptx::ex2_approx(x1);
+            if (ragged) {   // exact zeros for keys past N (also when scale == 0)
+              if (32 * c + i >= valid) p0 = 0.f;
+              if (32 * c + i + 1 >= valid) p1 = 0.f;
+            }
+            acc[(i >> 1) & 3] = ptx::f2_add(acc[(i >> 1) & 3], ptx::f2_pack(p0, p1));
+            pk[c >> 1][(c & 1) * 16 + (i >> 1)] = ptx::pack_bf16x2(p0, p1);
+          }
+        }
+        if (rescale_o) {
+  #pragma unroll
+          for (int c = 0; c < HD / 32; ++c) {
+            uint32_t o[32];
+            ptx::tmem_ld32(tO + 32 * c, o);
+            ptx::tmem_ld_wait();
+            ptx::reg_fence32(o);
+  #pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            ptx::tmem_st32(tO + 32 * c, o);
+          }
+        }
+        ptx::tmem_st32(tS, pk[0]);
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(ptx::smem_u32(&bar_p_half[t]));
+  #pragma unroll
+        for (int c = 2; c < 4; ++c) {
   #pragma unroll
           for (int i = 0; i < 32; i += 2) {
             float x0, x1;
@@ -819,20 +901,7 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
         const float pmax = ptx::ex2_approx(fmaf(mt, sl2, neg_m));
         l = l * alpha + sum;
         lo = lo * alpha + (sum + (ptx::round_bf16(pmax) - pmax));
-        ptx::tmem_st32(tS, pk[0]);
         ptx::tmem_st32(tS + 32, pk[1]);
-        if (rescale_o) {
-  #pragma unroll
-          for (int c = 0; c < HD / 32; ++c) {
-            uint32_t o[32];
-            ptx::tmem_ld32(tO + 32 * c, o);
-            ptx::tmem_ld_wait();
-            ptx::reg_fence32(o);
-  #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            ptx::tmem_st32(tO + 32 * c, o);
-          }
-        }
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         ptx::mbar_arrive(ptx::smem_u32(&bar_p_full[t]));

@@ -318,6 +318,27 @@ __device__ __forceinline__ void mma_ss_k64_warp(uint32_t d_tmem, uint32_t a_lo, 
   "setp.ne.b32 p, %5, 0;\n\tsetp.eq.u32 t, %4, %4;\n\telect.sync _|e, 0xffffffff;\n\t" \
   "mov.b64 bd, {%2, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n\t"
 
+#define FA_BURST_TS_HEAD_ACC \
+  "{\n\t.reg .pred e, t;\n\t.reg .b32 ta, bl;\n\t.reg .b64 bd;\n\t" \
+  "setp.eq.u32 t, %4, %4;\n\telect.sync _|e, 0xffffffff;\n\t"
+
+// Half of the 128-key P V burst (A columns step 8 per product): keys
+// [64 kHalf, 64 kHalf + 64), four products; the second half always accumulates.
+template <int kHalf>
+__device__ __forceinline__ void mma_ts_k64half_warp(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                                    uint32_t idesc, uint32_t acc0) {
+  if constexpr (kHalf == 0) {
+    asm volatile(FA_BURST_TS_HEAD FA_BURST_TS(8, 128) FA_BURST_TS(16, 256) FA_BURST_TS(24, 384) "}" ::"r"(d_tmem),
+                 "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc0)
+                 : "memory");
+  } else {
+    asm volatile(FA_BURST_TS_HEAD_ACC FA_BURST_TS(32, 512) FA_BURST_TS(40, 640) FA_BURST_TS(48, 768)
+                 FA_BURST_TS(56, 896) "}" ::"r"(d_tmem),
+                 "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc0)
+                 : "memory");
+  }
+}
+
 template <int kA4>
 __device__ __forceinline__ void mma_ts_k128_warp(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
                                                  uint32_t idesc, uint32_t acc0) {
