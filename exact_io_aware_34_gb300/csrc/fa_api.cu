@@ -59,6 +59,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // [B*H, N, d] bf16 view of a contiguous [B, H, N, d] tensor; box = 64 x 128
 // rows x 1 head, 128-byte swizzle. Rows beyond N of a head are outside the
 // tensor and read as zeros, so a ragged last block never sees the next head.
+bool make_map_ld(CUtensorMap* m, const void* base, int Z, int rows, int cols, long long ld, int box_cols,
+                 int box_rows);
 bool make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
   auto fn = encode_fn();
   if (!fn) return false;
@@ -186,9 +188,9 @@ fa_status_t launch(const void* Q, const void* K, const void* V, void* O, float* 
   if (fi->err != cudaSuccess) return cuda_fail(fi->err);
   if (!fi->regs_ok) return FA_ERR_UNSUPPORTED;
 
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if (!make_map(&mq, Q, B * H, N, HD) || !make_map(&mk, K, B * H_kv, N_kv, HD) ||
-      !make_map(&mv, V, B * H_kv, N_kv, HD))
+      !make_map(&mv, V, B * H_kv, N_kv, HD) || !make_map_ld(&mo, O, B * H, N, HD, HD, 64, 32))
     return cuda_fail(cudaErrorInvalidValue);
 
   fa::FwdParams p;
@@ -237,11 +239,11 @@ fa_status_t launch(const void* Q, const void* K, const void* V, void* O, float* 
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, fa::fa_fwd_kernel<HD>, mq, mk, mv, p);
+    e = cudaLaunchKernelEx(&cfg, fa::fa_fwd_kernel<HD>, mq, mk, mv, mo, p);
     if (e != cudaSuccess) return cuda_fail(e);
     return FA_OK;
   }
-  fa::fa_fwd_kernel<HD><<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, p);
+  fa::fa_fwd_kernel<HD><<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mo, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   return FA_OK;

@@ -73,7 +73,10 @@
 // Shared memory: Q tiles (2 x 128 x d bf16) + a ring of K/V tiles
 // (kStages x 128 x d bf16), each tile stored as d/64 chunks of 128 rows x
 // 128 bytes in the 128-byte swizzled layout that TMA writes and the tensor
-// core reads.
+// core reads, + one 4 KB O staging buffer per softmax warp (32 rows x 64
+// columns of bf16, the same layout): the epilogue writes O there chunk by
+// chunk and one lane stores each chunk with a tiled TMA store, instead of
+// every thread writing its own row to global memory.
 #pragma once
 
 #include <cuda.h>
@@ -102,7 +105,8 @@ struct FwdCfg {
   static constexpr int kStages = (HD == 128) ? 4 : 8;        // K/V ring slots
   static constexpr int kSmemQ = kQTiles * kTileBytes;
   static constexpr int kSmemKV = kStages * kTileBytes;
-  static constexpr int kSmemBytes = kSmemQ + kSmemKV + 1024;  // + alignment slack
+  static constexpr int kSmemStage = 8 * 32 * 128;  // per softmax warp: 32 rows x 64 columns of bf16 O
+  static constexpr int kSmemBytes = kSmemQ + kSmemKV + kSmemStage + 1024;  // + alignment slack
   static constexpr int kThreads = 384;          // 12 warps: 3 warpgroups
   // Registers per thread after the split: the two softmax warpgroups raise
   // theirs, the control warpgroup (producer, MMA issuer, two idle warps)
@@ -255,7 +259,8 @@ __device__ __forceinline__ TailPart tail_part(const FwdParams& p) {
 template <int HD>
 __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                  const FwdParams p) {
   using C = FwdCfg<HD>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_q_full;
@@ -293,6 +298,7 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
   const uint32_t smem_base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t sQ = smem_base;
   const uint32_t sKV = smem_base + C::kSmemQ;
+  const uint32_t sStage = sKV + C::kSmemKV;
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(ptx::smem_u32(&bar_q_full), 1);
@@ -729,25 +735,46 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
     if (ok) {
       ptx::tc_fence_after();
       const int bh = unit_head(u);
-      const int grow = unit_row0(u) + t * C::kBM + row;
+      const int row0 = unit_row0(u) + t * C::kBM + quarter * 32;   // this warp's first row
+      const int grow = row0 + lane;
       const bool in_range = grow < p.N;
       const float inv_l = 1.f / lo;
-      __nv_bfloat16* orow = p.O + (static_cast<size_t>(bh) * p.N + grow) * HD;
+      // O goes out through shared memory: each warp writes its 32 rows of a
+      // 64-column chunk in the 128-byte swizzled layout, then one lane stores
+      // them with a tiled TMA store (rows past N are not written).
+      if (row0 < p.N) {
+        const uint32_t stage = sStage + static_cast<uint32_t>(warp) * (32u * 128u);
 #pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
-        uint32_t o[32];
-        ptx::tmem_ld32(tO + 32 * c, o);
-        ptx::tmem_ld_wait();
-        ptx::reg_fence32(o);
-        uint32_t packed[16];
+        for (int k = 0; k < HD / 64; ++k) {
+          // The staging rows are free once this warp's previous store has read them.
+          if (lane == 0) ptx::bulk_wait_group_read0();
+          __syncwarp();
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          packed[i] = ptx::pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-        if (in_range) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+          for (int h = 0; h < 2; ++h) {
+            uint32_t o[32];
+            ptx::tmem_ld32(tO + 64 * k + 32 * h, o);
+            ptx::tmem_ld_wait();
+            ptx::reg_fence32(o);
+            uint32_t packed[16];
 #pragma unroll
-          for (int v = 0; v < 4; ++v)
-            dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+            for (int i = 0; i < 16; ++i)
+              packed[i] = ptx::pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+            const uint32_t row_addr = stage + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const uint32_t unit = 4u * h + v;      // 16-byte unit within the 128-byte row
+              const uint32_t addr = row_addr + ((unit ^ static_cast<uint32_t>(lane & 7)) << 4);
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(packed[4 * v]),
+                           "r"(packed[4 * v + 1]), "r"(packed[4 * v + 2]), "r"(packed[4 * v + 3])
+                           : "memory");
+            }
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_3d(&tmO, stage, 64 * k, row0, bh);
+            ptx::bulk_commit_group();
+          }
         }
       }
       if (in_range) {
@@ -975,6 +1002,9 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
     }
   }
 
+  // The O stores must have read the staging rows before the CTA's shared
+  // memory is released.
+  if (warp < 8 && lane == 0) ptx::bulk_wait_group_read0();
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 9) {
