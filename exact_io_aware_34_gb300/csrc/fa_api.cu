@@ -431,9 +431,10 @@ fa_status_t bwd_launch(const void* Q, const void* K, const void* V, const void* 
   if (attr_err[dev] != cudaSuccess) return cuda_fail(attr_err[dev]);
 
   const int BH = B * H;
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, mdq, mdk, mdv;
   if (!make_map(&mq, Q, BH, N, HD) || !make_map(&mk, K, BH, N, HD) || !make_map(&mv, V, BH, N, HD) ||
-      !make_map(&mdo, dO, BH, N, HD))
+      !make_map(&mdo, dO, BH, N, HD) || !make_map_ld(&mdq, dQ, BH, N, HD, HD, 64, 32) ||
+      !make_map_ld(&mdk, dK, BH, N, HD, HD, 64, 32) || !make_map_ld(&mdv, dV, BH, N, HD, HD, 64, 32))
     return cuda_fail(cudaErrorInvalidValue);
 
   const long long npad = bwd_npad(N);
@@ -463,7 +464,7 @@ fa_status_t bwd_launch(const void* Q, const void* K, const void* V, const void* 
   // 2. dK and dV (one CTA per 128 key rows), then dQ (one CTA per 128 query
   // rows), in one launch
   const unsigned ctas = static_cast<unsigned>(2LL * p.n_blocks * BH);
-  fa::fa_bwd_kernel<HD><<<ctas, C::kThreads, kSmem, stream>>>(mq, mk, mv, mdo, p);
+  fa::fa_bwd_kernel<HD><<<ctas, C::kThreads, kSmem, stream>>>(mq, mk, mv, mdo, mdq, mdk, mdv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   return FA_OK;

@@ -59,6 +59,10 @@
 // so that no warp overwrites scores another warp has yet to load. For the
 // tile products that read them, key step kk (16 streamed rows) sits at
 // column 64 (kk >> 2) + 8 (kk & 3).
+// At d = 128 the gradients leave through shared memory, which is free once
+// the CTA's last products have completed: each elementwise warp writes its
+// 32 rows x 64 columns in the 128-byte swizzled layout and one lane stores
+// them with a tiled TMA store, instead of every thread writing its own row.
 #pragma once
 
 #include "fa_fwd_kernel.cuh"
@@ -216,6 +220,33 @@ __device__ __forceinline__ void store_row32(uint32_t taddr, float mul, __nv_bflo
   }
 }
 
+// Epilogue helper for d = 128, once every product of the CTA has completed
+// (its shared memory is free then): the warp's 32 rows x 64 columns of an
+// accumulator, times `mul`, to bf16 in a 4 KB staging buffer at `stage`, in
+// the 128-byte swizzled layout a tiled TMA store reads.
+__device__ __forceinline__ void stage_rows64(uint32_t taddr, float mul, uint32_t stage, int lane) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t v[32];
+    ptx::tmem_ld32(taddr + 32 * h, v);
+    ptx::tmem_ld_wait();
+    ptx::reg_fence32(v);
+    uint32_t packed[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      packed[i] = ptx::pack_bf16x2(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
+    const uint32_t row_addr = stage + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t unit = 4u * h + q;      // 16-byte unit within the 128-byte row
+      const uint32_t addr = row_addr + ((unit ^ static_cast<uint32_t>(lane & 7)) << 4);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(packed[4 * q]),
+                   "r"(packed[4 * q + 1]), "r"(packed[4 * q + 2]), "r"(packed[4 * q + 3])
+                   : "memory");
+    }
+  }
+}
+
 // ---------------------------------------------------------------- dQ
 // Shared memory: Q and dO of the CTA's query block, a ring of kKSlots K tiles
 // and one of kVSlots V tiles (K_j is read twice, by S_j early and by dQ_j
@@ -240,6 +271,7 @@ struct DqCfg {
 // head bh. The tensor maps are the kernel's own (grid-constant) parameters.
 template <int HD>
 __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                           const CUtensorMap& tmdQ,
                                            const CUtensorMap& tmdO, const BwdParams& p, int blk, int bh) {
   using C = BwdCfg<HD>;
   using D = DqCfg<HD>;
@@ -500,11 +532,29 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tmQ, const CUtenso
     if (ok) ok = wait_warp_or_abort(ptx::smem_u32(&bar_acc_full), 0, abort_ptr, p.timeout_ns, kRoleDqSoftmax);
     if (ok) {
       ptx::tc_fence_after();
-      const int q = q0 + row;
-      __nv_bfloat16* dst = p.dQ + (static_cast<size_t>(bh) * p.N + q) * HD + half * (HD / 2);
+      if constexpr (HD == 128) {
+        // Through shared memory: 32 rows x 64 columns per warp, then one
+        // tiled TMA store (rows past N are not written).
+        const int qw = q0 + quarter * 32;
+        if (qw < p.N) {
+          const uint32_t stage = smem_base + static_cast<uint32_t>(warp) * 4096u;
+          stage_rows64(tmem_base + lane_addr + D::kColDQ + half * 64, p.scale, stage, lane);
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_3d(&tmdQ, stage, half * 64, qw, bh);
+            ptx::bulk_commit_group();
+            ptx::bulk_wait_group_read0();
+          }
+          __syncwarp();
+        }
+      } else {
+        const int q = q0 + row;
+        __nv_bfloat16* dst = p.dQ + (static_cast<size_t>(bh) * p.N + q) * HD + half * (HD / 2);
 #pragma unroll
-      for (int c = 0; c < HD / 64; ++c)
-        store_row32(tmem_base + lane_addr + D::kColDQ + half * (HD / 2) + 32 * c, p.scale, dst + 32 * c, q < p.N);
+        for (int c = 0; c < HD / 64; ++c)
+          store_row32(tmem_base + lane_addr + D::kColDQ + half * (HD / 2) + 32 * c, p.scale, dst + 32 * c, q < p.N);
+      }
     }
   }
 
@@ -520,6 +570,7 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tmQ, const CUtenso
 // One CTA of the key-block role: key rows [128 blk, 128 blk + 128) of head bh.
 template <int HD>
 __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                             const CUtensorMap& tmdK, const CUtensorMap& tmdV,
                                              const CUtensorMap& tmdO, const BwdParams& p, int blk, int bh) {
   using C = BwdCfg<HD>;
   constexpr uint32_t kColDV = 0;
@@ -823,13 +874,33 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
     if (ok) ok = wait_warp_or_abort(ptx::smem_u32(&bar_acc_full), 0, abort_ptr, p.timeout_ns, kRoleDkvSoftmax);
     if (ok) {
       ptx::tc_fence_after();
-      const int kv = kv0 + row;
-      const size_t off = (static_cast<size_t>(bh) * p.N + kv) * HD + half * (HD / 2);
+      if constexpr (HD == 128) {
+        // Through shared memory: per warp 32 rows x 64 columns of dV and of
+        // dK, then two tiled TMA stores (rows past N are not written).
+        const int kw = kv0 + quarter * 32;
+        if (kw < p.N) {
+          const uint32_t stage = smem_base + static_cast<uint32_t>(warp) * 8192u;
+          stage_rows64(tmem_base + lane_addr + kColDV + half * 64, 1.f, stage, lane);
+          stage_rows64(tmem_base + lane_addr + kColDK + half * 64, p.scale, stage + 4096u, lane);
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_3d(&tmdV, stage, half * 64, kw, bh);
+            ptx::tma_store_3d(&tmdK, stage + 4096u, half * 64, kw, bh);
+            ptx::bulk_commit_group();
+            ptx::bulk_wait_group_read0();
+          }
+          __syncwarp();
+        }
+      } else {
+        const int kv = kv0 + row;
+        const size_t off = (static_cast<size_t>(bh) * p.N + kv) * HD + half * (HD / 2);
 #pragma unroll
-      for (int c = 0; c < HD / 64; ++c) {
-        store_row32(tmem_base + lane_addr + kColDV + half * (HD / 2) + 32 * c, 1.f, p.dV + off + 32 * c, kv < p.N);
-        store_row32(tmem_base + lane_addr + kColDK + half * (HD / 2) + 32 * c, p.scale, p.dK + off + 32 * c,
-                    kv < p.N);
+        for (int c = 0; c < HD / 64; ++c) {
+          store_row32(tmem_base + lane_addr + kColDV + half * (HD / 2) + 32 * c, 1.f, p.dV + off + 32 * c, kv < p.N);
+          store_row32(tmem_base + lane_addr + kColDK + half * (HD / 2) + 32 * c, p.scale, p.dK + off + 32 * c,
+                      kv < p.N);
+        }
       }
     }
   }
@@ -851,7 +922,8 @@ template <int HD>
 __global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                  const BwdParams p) {
+                  const __grid_constant__ CUtensorMap tmdQ, const __grid_constant__ CUtensorMap tmdK,
+                  const __grid_constant__ CUtensorMap tmdV, const BwdParams p) {
   // The CTAs of one head are consecutive: its key-block CTAs (the longer
   // role first), then its query-block CTAs. Both roles stream that head's Q,
   // K, V and dO, which then stay in L2 from one role to the other.
@@ -862,9 +934,9 @@ __global__ void __launch_bounds__(BwdCfg<HD>::kThreads, 1)
   const bool dkdv = r < p.n_blocks;
   const int blk = dkdv ? r : r - p.n_blocks;
   if (dkdv)
-    bwd_dkdv_cta<HD>(tmQ, tmK, tmV, tmdO, p, blk, bh);
+    bwd_dkdv_cta<HD>(tmQ, tmK, tmV, tmdK, tmdV, tmdO, p, blk, bh);
   else
-    bwd_dq_cta<HD>(tmQ, tmK, tmV, tmdO, p, blk, bh);
+    bwd_dq_cta<HD>(tmQ, tmK, tmV, tmdQ, tmdO, p, blk, bh);
 }
 
 }  // namespace fa
