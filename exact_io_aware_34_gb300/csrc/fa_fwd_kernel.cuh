@@ -440,7 +440,8 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
     // issues far more slowly while the softmax warps of its sub-partition
     // compete for issue slots.
     // P V for query tile t from the V tile loaded as the it-th K/V load (P_t
-    // sits in the S_t columns); the first product of a unit overwrites O_t.
+    // sits in the S_t columns), over keys [64 half, 64 half + 64): four
+    // K = 16 products; the first product of a unit overwrites O_t.
     auto issue_pv_half = [&](int t, int it, bool accumulate, int half) {
       const uint32_t v_tile = sKV + (it % C::kStages) * C::kTileBytes;
       const uint32_t d_tmem = tmem_base + C::kColO + HD * t;
@@ -467,10 +468,9 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
     // Per unit: Q and K_0 are waited for here; every later K_{j+1} and V_j
     // is waited for by the softmax warps before their first hand-off for
     // block j (p_half), so the p_half / p_full waits below imply those tiles
-    // have landed. An
-    // mbarrier wait in this warp stalls the queued tensor-core work, so it
-    // does as few as it can. g counts the key blocks of all units so far
-    // (the phase of s_full / p_full).
+    // have landed. An mbarrier wait in this warp stalls the queued
+    // tensor-core work, so it does as few as it can. g counts the key blocks
+    // of all units so far (the phase of s_full, p_half and p_full).
     bool ok = true;
     int g = 0, uc = 0;
     for (int u = blockIdx.x; u < p.num_whole && ok; u += gridDim.x, ++uc) {

@@ -318,6 +318,8 @@ __device__ __forceinline__ void mma_ss_k64_warp(uint32_t d_tmem, uint32_t a_lo, 
   "setp.ne.b32 p, %5, 0;\n\tsetp.eq.u32 t, %4, %4;\n\telect.sync _|e, 0xffffffff;\n\t" \
   "mov.b64 bd, {%2, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n\t"
 
+// Opens a burst whose products all accumulate (no leading product that may
+// overwrite D): the continuation of a burst split in two.
 #define FA_BURST_TS_HEAD_ACC \
   "{\n\t.reg .pred e, t;\n\t.reg .b32 ta, bl;\n\t.reg .b64 bd;\n\t" \
   "setp.eq.u32 t, %4, %4;\n\telect.sync _|e, 0xffffffff;\n\t"
