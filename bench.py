@@ -39,6 +39,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -64,11 +65,20 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 
 
 # ----------------------------------------------------------------------------- helpers
+def _code_only(text: str) -> str:
+    """C++ source without its comments and with runs of whitespace collapsed,
+    so that an edit of comments alone leaves the hash (and the machine code)
+    unchanged. The kernels' string literals hold no comment markers."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(sources=None) -> str:
     h = hashlib.sha256()
     for rel in (KERNEL_SOURCES if sources is None else sources):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

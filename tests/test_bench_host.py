@@ -102,6 +102,17 @@ def test_cpu_baseline_single_core():
     assert r["workload"] == "n256_d64"
 
 
+def test_source_hash_ignores_comments_only():
+    """The DRAM records are keyed by a hash of the kernel sources' code: an
+    edit of comments or layout keeps it, an edit of code changes it."""
+    a = "int f(int x) {\n  // one\n  return x + 1; /* two\n lines */\n}\n"
+    b = "int f(int x) {   return x + 1;\n\n}  // other words\n"
+    c = "int f(int x) {\n  return x + 2;\n}\n"
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
+    assert "asm(\"mov.b32 %0, %1;\")" in bench._code_only('asm("mov.b32 %0, %1;") // note')
+
+
 def test_committed_traffic_records_match_their_profiles():
     """Each record of profiles/dram_traffic.json adds up, and the ncu summary it
     comes from names the same kernel-sources hash. Where the record is current
