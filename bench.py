@@ -59,6 +59,7 @@ BWD_KERNEL_SOURCES = ["exact_io_aware_34_gb300/csrc/fa_bwd_kernel.cuh", "exact_i
                       "exact_io_aware_34_gb300/csrc/sm103a_ptx.cuh"]
 DECODE_KERNEL_SOURCES = ["exact_io_aware_34_gb300/csrc/fa_decode_kernel.cuh", "exact_io_aware_34_gb300/csrc/fa_fwd_kernel.cuh",
                          "exact_io_aware_34_gb300/csrc/sm103a_ptx.cuh"]
+NAIVE_KERNEL_SOURCES = ["exact_io_aware_34_gb300/csrc/naive_kernels.cuh", "exact_io_aware_34_gb300/csrc/sm103a_ptx.cuh"]
 DECODE_WORKLOAD = "decode32k_gqa8_b4"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
@@ -691,7 +692,8 @@ def run_native(args):
             "roofline": {"bound": "hbm", "achieved": n_bytes / (naive_ms * 1e-3) / 1e9, "peak": peaks_c["hbm_gbs"],
                          "unit": "GB/s", "frac": n_bytes / (naive_ms * 1e-3) / 1e9 / peaks_c["hbm_gbs"],
                          "algorithmic_bytes_per_call": n_bytes, "peak_source": f"{peak_src_c} HBM copy bandwidth",
-                         "kernels": "gemm_bf16_kernel<128, 1> (S), softmax_rows_kernel, gemm_bf16_kernel<d, 0> (PV)"},
+                         "traffic": load_traffic(w.name, ":comparator", NAIVE_KERNEL_SOURCES),
+                         "kernels": "s_gemm_kernel (S, persistent), softmax_rows_kernel, gemm_bf16_kernel<d, 0> (PV)"},
         }
         del ws, o_n, lse_n
         torch.cuda.empty_cache()

@@ -129,6 +129,7 @@ def test_committed_traffic_records_match_their_profiles():
         "long32k_d128_h16_spiky": "dram_traffic_all_workloads.md",
         "prefill8k_d128_h32:bwd": "fa_bwd_kernels_prefill8k_d128.md",
         "decode32k_gqa8_b4": "fa_decode_kernel_decode32k_gqa8.md",
+        "prefill8k_d128_h32:comparator": "dram_traffic_all_workloads.md",
     }
     assert set(rec) == set(summaries)
     for key, md in summaries.items():
