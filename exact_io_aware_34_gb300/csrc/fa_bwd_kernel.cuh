@@ -175,6 +175,56 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
   }
 }
 
+// The tile-product bursts of sm103a_ptx.cuh (mma_ss_k128_warp, mma_ss_k64_warp,
+// mma_ts_k128_warp) with each product's descriptors formed by one 64-bit add
+// to the burst's base descriptors: the offsets never carry out of the
+// start-address field, so the descriptor words are the same. That takes
+// fewer instructions from the issuing warp, which shares its sub-partition
+// with elementwise warps; here it made the backward call 2.5 % faster, while
+// the forward kernel measured no better with it.
+#define FA_BURST_SS64(OA) "add.s64 ad, a0, " #OA ";\n\tadd.s64 bd, b0, " #OA ";\n\t" \
+  "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %4, t;\n\t"
+#define FA_BURST_SS64_HEAD \
+  "{\n\t.reg .pred p, e, t;\n\t.reg .b64 a0, b0, ad, bd;\n\t" \
+  "setp.ne.b32 p, %5, 0;\n\tsetp.eq.u32 t, %4, %4;\n\telect.sync _|e, 0xffffffff;\n\t" \
+  "mov.b64 a0, {%1, %3};\n\tmov.b64 b0, {%2, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], a0, b0, %4, p;\n\t"
+#define FA_BURST_TS64(OA, OB) "add.u32 ta, %1, " #OA ";\n\tadd.s64 bd, b0, " #OB ";\n\t" \
+  "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], bd, %4, t;\n\t"
+#define FA_BURST_TS64_HEAD \
+  "{\n\t.reg .pred p, e, t;\n\t.reg .b32 ta;\n\t.reg .b64 b0, bd;\n\t" \
+  "setp.ne.b32 p, %5, 0;\n\tsetp.eq.u32 t, %4, %4;\n\telect.sync _|e, 0xffffffff;\n\t" \
+  "mov.b64 b0, {%2, %3};\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b0, %4, p;\n\t"
+
+__device__ __forceinline__ void mma_ss_k128_warp64(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                                                   uint32_t idesc, uint32_t acc0) {
+  asm volatile(FA_BURST_SS64_HEAD FA_BURST_SS64(2) FA_BURST_SS64(4) FA_BURST_SS64(6) FA_BURST_SS64(1024)
+               FA_BURST_SS64(1026) FA_BURST_SS64(1028) FA_BURST_SS64(1030) "}" ::"r"(d_tmem),
+               "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(acc0)
+               : "memory");
+}
+__device__ __forceinline__ void mma_ss_k64_warp64(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                                                  uint32_t idesc, uint32_t acc0) {
+  asm volatile(FA_BURST_SS64_HEAD FA_BURST_SS64(2) FA_BURST_SS64(4) FA_BURST_SS64(6) "}" ::"r"(d_tmem), "r"(a_lo),
+               "r"(b_lo), "r"(hi), "r"(idesc), "r"(acc0)
+               : "memory");
+}
+template <int kA4>
+__device__ __forceinline__ void mma_ts_k128_warp64(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                                   uint32_t idesc, uint32_t acc0) {
+  static_assert(kA4 == 32 || kA4 == 64, "A column step of the second four products");
+  if constexpr (kA4 == 32) {
+    asm volatile(FA_BURST_TS64_HEAD FA_BURST_TS64(8, 128) FA_BURST_TS64(16, 256) FA_BURST_TS64(24, 384)
+                 FA_BURST_TS64(32, 512) FA_BURST_TS64(40, 640) FA_BURST_TS64(48, 768) FA_BURST_TS64(56, 896) "}"
+                 ::"r"(d_tmem), "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc0)
+                 : "memory");
+  } else {
+    asm volatile(FA_BURST_TS64_HEAD FA_BURST_TS64(8, 128) FA_BURST_TS64(16, 256) FA_BURST_TS64(24, 384)
+                 FA_BURST_TS64(64, 512) FA_BURST_TS64(72, 640) FA_BURST_TS64(80, 768) FA_BURST_TS64(88, 896) "}"
+                 ::"r"(d_tmem), "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc0)
+                 : "memory");
+  }
+}
+
 // S-shaped product over the model dimension: D[128 x 128] = A B^T with A and
 // B two 128-row tiles in the K-major swizzled layout (k = 0 .. HD). Called by
 // the whole converged issuer warp (one elected lane issues).
@@ -184,9 +234,9 @@ __device__ __forceinline__ void issue_tile_qk(uint32_t d_tmem, uint32_t a_tile, 
   static_assert(C::kChunkBytes == 16384, "128-row tiles of 128-byte rows per chunk");
   const uint64_t a_desc = ptx::desc_kmajor_sw128(a_tile), b_desc = ptx::desc_kmajor_sw128(b_tile);
   if constexpr (HD == 128)
-    ptx::mma_ss_k128_warp(d_tmem, ptx::desc_lo(a_desc), ptx::desc_lo(b_desc), ptx::desc_hi(a_desc), C::kIdescS, 0u);
+    mma_ss_k128_warp64(d_tmem, ptx::desc_lo(a_desc), ptx::desc_lo(b_desc), ptx::desc_hi(a_desc), C::kIdescS, 0u);
   else
-    ptx::mma_ss_k64_warp(d_tmem, ptx::desc_lo(a_desc), ptx::desc_lo(b_desc), ptx::desc_hi(a_desc), C::kIdescS, 0u);
+    mma_ss_k64_warp64(d_tmem, ptx::desc_lo(a_desc), ptx::desc_lo(b_desc), ptx::desc_hi(a_desc), C::kIdescS, 0u);
 }
 
 // Accumulating product over the 128 streamed rows: D[128 x HD] += A B with A
@@ -197,7 +247,7 @@ template <int HD, int kHalf>
 __device__ __forceinline__ void issue_tile_acc(uint32_t d_tmem, uint32_t a_col, uint32_t b_tile, bool accumulate) {
   using C = BwdCfg<HD>;
   const uint64_t b_desc = ptx::desc_mnmajor_sw128(b_tile, C::kChunkBytes);
-  ptx::mma_ts_k128_warp<kHalf>(d_tmem, a_col, ptx::desc_lo(b_desc), ptx::desc_hi(b_desc), C::kIdescAcc,
+  mma_ts_k128_warp64<kHalf>(d_tmem, a_col, ptx::desc_lo(b_desc), ptx::desc_hi(b_desc), C::kIdescAcc,
                                accumulate ? 1u : 0u);
 }
 
