@@ -800,6 +800,9 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tmQ, const CUten
             if (__all_sync(0xffffffffu, ptx::mbar_test_wait(ptx::smem_u32(&bar_p_full), i & 1))) break;
             // Out of time or aborting: the bounded wait below reports it.
             if (__any_sync(0xffffffffu, *abort_ptr != 0) || ptx::globaltimer_ns() - t0 > p.timeout_ns) break;
+            // Poll less often: the elementwise warps of this sub-partition
+            // need the issue slots meanwhile.
+            __nanosleep(32);
           }
         }
         ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_full), i & 1, abort_ptr, p.timeout_ns, kRoleDkvMma);
