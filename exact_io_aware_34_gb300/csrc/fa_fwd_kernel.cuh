@@ -659,22 +659,61 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
       const uint64_t negmx2 = ptx::f2_pack(neg_m, neg_m);
       uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
       uint32_t pk[2][32];
+      // At d = 64 the pass is written twice, with and without the ragged
+      // block's masking (+6 % at d = 64; the same split cost 3 % at d = 128,
+      // which keeps one loop with the test inside).
+      if constexpr (HD == 64) {
+        if (!ragged) {
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+          for (int c = 0; c < 2; ++c) {
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float x0, x1;
-          ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[c][i]), __uint_as_float(s[c][i + 1])), sl2x2,
-                                     negmx2),
-                         x0, x1);
-          float p0 = ptx::ex2_approx(x0);
-          float p1 = ptx::ex2_approx(x1);
-          if (ragged) {   // exact zeros for keys past N (also when scale == 0)
-            if (32 * c + i >= valid) p0 = 0.f;
-            if (32 * c + i + 1 >= valid) p1 = 0.f;
+            for (int i = 0; i < 32; i += 2) {
+              float x0, x1;
+              ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[c][i]), __uint_as_float(s[c][i + 1])), sl2x2,
+                                         negmx2),
+                             x0, x1);
+              float p0 = ptx::ex2_approx(x0);
+              float p1 = ptx::ex2_approx(x1);
+              acc[(i >> 1) & 3] = ptx::f2_add(acc[(i >> 1) & 3], ptx::f2_pack(p0, p1));
+              pk[c >> 1][(c & 1) * 16 + (i >> 1)] = ptx::pack_bf16x2(p0, p1);
+            }
           }
-          acc[(i >> 1) & 3] = ptx::f2_add(acc[(i >> 1) & 3], ptx::f2_pack(p0, p1));
-          pk[c >> 1][(c & 1) * 16 + (i >> 1)] = ptx::pack_bf16x2(p0, p1);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              float x0, x1;
+              ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[c][i]), __uint_as_float(s[c][i + 1])), sl2x2,
+                                         negmx2),
+                             x0, x1);
+              float p0 = ptx::ex2_approx(x0);
+              float p1 = ptx::ex2_approx(x1);
+              if (32 * c + i >= valid) p0 = 0.f;   // keys past N: exact zeros (also when scale == 0)
+              if (32 * c + i + 1 >= valid) p1 = 0.f;
+              acc[(i >> 1) & 3] = ptx::f2_add(acc[(i >> 1) & 3], ptx::f2_pack(p0, p1));
+              pk[c >> 1][(c & 1) * 16 + (i >> 1)] = ptx::pack_bf16x2(p0, p1);
+            }
+          }
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float x0, x1;
+            ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[c][i]), __uint_as_float(s[c][i + 1])), sl2x2,
+                                       negmx2),
+                           x0, x1);
+            float p0 = ptx::ex2_approx(x0);
+            float p1 = ptx::ex2_approx(x1);
+            if (ragged) {   // exact zeros for keys past N (also when scale == 0)
+              if (32 * c + i >= valid) p0 = 0.f;
+              if (32 * c + i + 1 >= valid) p1 = 0.f;
+            }
+            acc[(i >> 1) & 3] = ptx::f2_add(acc[(i >> 1) & 3], ptx::f2_pack(p0, p1));
+            pk[c >> 1][(c & 1) * 16 + (i >> 1)] = ptx::pack_bf16x2(p0, p1);
+          }
         }
       }
       if (rescale_o) {
@@ -693,22 +732,58 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       ptx::mbar_arrive(ptx::smem_u32(&bar_p_half[t]));
+      if constexpr (HD == 64) {
+        if (!ragged) {
 #pragma unroll
-      for (int c = 2; c < 4; ++c) {
+          for (int c = 2; c < 4; ++c) {
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float x0, x1;
-          ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[c][i]), __uint_as_float(s[c][i + 1])), sl2x2,
-                                     negmx2),
-                         x0, x1);
-          float p0 = ptx::ex2_approx(x0);
-          float p1 = ptx::ex2_approx(x1);
-          if (ragged) {   // exact zeros for keys past N (also when scale == 0)
-            if (32 * c + i >= valid) p0 = 0.f;
-            if (32 * c + i + 1 >= valid) p1 = 0.f;
+            for (int i = 0; i < 32; i += 2) {
+              float x0, x1;
+              ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[c][i]), __uint_as_float(s[c][i + 1])), sl2x2,
+                                         negmx2),
+                             x0, x1);
+              float p0 = ptx::ex2_approx(x0);
+              float p1 = ptx::ex2_approx(x1);
+              acc[(i >> 1) & 3] = ptx::f2_add(acc[(i >> 1) & 3], ptx::f2_pack(p0, p1));
+              pk[c >> 1][(c & 1) * 16 + (i >> 1)] = ptx::pack_bf16x2(p0, p1);
+            }
           }
-          acc[(i >> 1) & 3] = ptx::f2_add(acc[(i >> 1) & 3], ptx::f2_pack(p0, p1));
-          pk[c >> 1][(c & 1) * 16 + (i >> 1)] = ptx::pack_bf16x2(p0, p1);
+        } else {
+#pragma unroll
+          for (int c = 2; c < 4; ++c) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              float x0, x1;
+              ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[c][i]), __uint_as_float(s[c][i + 1])), sl2x2,
+                                         negmx2),
+                             x0, x1);
+              float p0 = ptx::ex2_approx(x0);
+              float p1 = ptx::ex2_approx(x1);
+              if (32 * c + i >= valid) p0 = 0.f;   // keys past N: exact zeros (also when scale == 0)
+              if (32 * c + i + 1 >= valid) p1 = 0.f;
+              acc[(i >> 1) & 3] = ptx::f2_add(acc[(i >> 1) & 3], ptx::f2_pack(p0, p1));
+              pk[c >> 1][(c & 1) * 16 + (i >> 1)] = ptx::pack_bf16x2(p0, p1);
+            }
+          }
+        }
+      } else {
+#pragma unroll
+        for (int c = 2; c < 4; ++c) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float x0, x1;
+            ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[c][i]), __uint_as_float(s[c][i + 1])), sl2x2,
+                                       negmx2),
+                           x0, x1);
+            float p0 = ptx::ex2_approx(x0);
+            float p1 = ptx::ex2_approx(x1);
+            if (ragged) {   // exact zeros for keys past N (also when scale == 0)
+              if (32 * c + i >= valid) p0 = 0.f;
+              if (32 * c + i + 1 >= valid) p1 = 0.f;
+            }
+            acc[(i >> 1) & 3] = ptx::f2_add(acc[(i >> 1) & 3], ptx::f2_pack(p0, p1));
+            pk[c >> 1][(c & 1) * 16 + (i >> 1)] = ptx::pack_bf16x2(p0, p1);
+          }
         }
       }
       float sum;
