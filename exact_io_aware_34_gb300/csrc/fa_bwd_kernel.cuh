@@ -527,22 +527,37 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tmQ, const CUtenso
       const int valid = p.N - j * C::kBlk - 64 * half;   // keys of this warp's 64 that exist
       const bool ragged = valid < 64;
       // P (float32, kept in s) while dP_j is still on the tensor core.
+      if (!ragged) {
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < 2; ++c) {
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          float x0, x1;
-          ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[c][2 * k]), __uint_as_float(s[c][2 * k + 1])),
-                                     sl2x2, nlx2),
-                         x0, x1);
-          float p0 = ptx::ex2_approx(x0);
-          float p1 = ptx::ex2_approx(x1);
-          if (ragged) {   // keys past N: exact zeros whatever the fill gave
-            if (32 * c + 2 * k >= valid) p0 = 0.f;
-            if (32 * c + 2 * k + 1 >= valid) p1 = 0.f;
+          for (int k = 0; k < 16; ++k) {
+            float x0, x1;
+            ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[c][2 * k]), __uint_as_float(s[c][2 * k + 1])),
+                                       sl2x2, nlx2),
+                           x0, x1);
+            float p0 = ptx::ex2_approx(x0);
+            float p1 = ptx::ex2_approx(x1);
+            s[c][2 * k] = __float_as_uint(p0);
+            s[c][2 * k + 1] = __float_as_uint(p1);
           }
-          s[c][2 * k] = __float_as_uint(p0);
-          s[c][2 * k + 1] = __float_as_uint(p1);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            float x0, x1;
+            ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[c][2 * k]), __uint_as_float(s[c][2 * k + 1])),
+                                       sl2x2, nlx2),
+                           x0, x1);
+            float p0 = ptx::ex2_approx(x0);
+            float p1 = ptx::ex2_approx(x1);
+            if (32 * c + 2 * k >= valid) p0 = 0.f;   // keys past N: exact zeros whatever the fill gave
+            if (32 * c + 2 * k + 1 >= valid) p1 = 0.f;
+            s[c][2 * k] = __float_as_uint(p0);
+            s[c][2 * k + 1] = __float_as_uint(p1);
+          }
         }
       }
       ok = wait_warp_or_abort(ptx::smem_u32(&bar_dpt_full), j & 1, abort_ptr, p.timeout_ns, kRoleDqSoftmax);
