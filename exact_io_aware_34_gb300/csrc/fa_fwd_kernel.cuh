@@ -145,13 +145,18 @@ constexpr float kRescaleLog2 = 8.0f;
 
 // Bounded wait. Returns false when the CTA is aborting (another role gave up)
 // or when this wait itself ran out of time, in which case it raises the abort
-// flag and records the timeout in the device status word.
+// flag and records the timeout in the device status word. The flag and the
+// clock are read once per kPolls polls of the barrier: a phase that completes
+// while they are being read is seen only at the next poll.
+template <int kPolls = 1>
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                               unsigned long long timeout_ns, unsigned int role) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   while (true) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+    for (int r = 0; r < kPolls; ++r)
+      if (ptx::mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
     if (ptx::globaltimer_ns() - t0 > timeout_ns) {
       *abort_flag = 1;
@@ -170,13 +175,16 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
 // Warp-uniform bounded wait for the 32 lanes of a softmax warp: returns the
 // same answer in every lane, so the warp-collective TMEM instructions that
 // follow are never reached by part of a warp.
+template <int kPolls = 1>
 __device__ __forceinline__ bool wait_warp_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                                    unsigned long long timeout_ns, unsigned int role) {
   if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   const int lane = threadIdx.x & 31;
   while (true) {
-    if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
+#pragma unroll 1
+    for (int r = 0; r < kPolls; ++r)
+      if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
     int stop = 0;
     if (lane == 0) {
       if (*abort_flag) {
@@ -262,6 +270,10 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                   const FwdParams p) {
   using C = FwdCfg<HD>;
+  // Bounded waits read the abort flag and the clock once per this many polls
+  // (at d = 128 the hand-offs are then seen sooner; at d = 64 one poll per
+  // check measured faster).
+  constexpr int kPolls = HD == 128 ? 8 : 1;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_q_full;
   __shared__ __align__(8) uint64_t bar_q_empty;
@@ -351,7 +363,7 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
       for (int u = blockIdx.x; u < p.num_whole && ok; u += gridDim.x, ++uc) {
         const int bh = unit_head(u), bh_kv = kv_head(bh), q_row0 = unit_row0(u);
         // The previous unit's Q tiles are free once its last Q K^T products completed.
-        if (uc > 0 && !wait_or_abort(ptx::smem_u32(&bar_q_empty), (uc - 1) & 1, abort_ptr, p.timeout_ns,
+        if (uc > 0 && !wait_or_abort<kPolls>(ptx::smem_u32(&bar_q_empty), (uc - 1) & 1, abort_ptr, p.timeout_ns,
                                      kRoleProducer)) {
           ok = false;
           break;
@@ -367,7 +379,7 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
             const int it = 2 * n_kv * uc + 2 * j + kv;
             const int slot = it % C::kStages;
             const uint32_t phase = (it / C::kStages) & 1;
-            if (!wait_or_abort(ptx::smem_u32(&bar_kv_empty[slot]), phase ^ 1u, abort_ptr, p.timeout_ns,
+            if (!wait_or_abort<kPolls>(ptx::smem_u32(&bar_kv_empty[slot]), phase ^ 1u, abort_ptr, p.timeout_ns,
                                kRoleProducer)) {
               ok = false;
               break;
@@ -386,7 +398,7 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
       if (const TailPart tp = tail_part(p); ok && tp.valid) {
         // The split unit: Q, then this CTA's half of the key blocks.
         const int bh = unit_head(tp.u), bh_kv = kv_head(bh), q_row0 = unit_row0(tp.u);
-        if (uc > 0 && !wait_or_abort(ptx::smem_u32(&bar_q_empty), (uc - 1) & 1, abort_ptr, p.timeout_ns,
+        if (uc > 0 && !wait_or_abort<kPolls>(ptx::smem_u32(&bar_q_empty), (uc - 1) & 1, abort_ptr, p.timeout_ns,
                                      kRoleProducer))
           ok = false;
         if (ok) {
@@ -402,7 +414,7 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
             const int it = 2 * n_kv * uc + 2 * (j - tp.kb0) + kv;
             const int slot = it % C::kStages;
             const uint32_t phase = (it / C::kStages) & 1;
-            if (!wait_or_abort(ptx::smem_u32(&bar_kv_empty[slot]), phase ^ 1u, abort_ptr, p.timeout_ns,
+            if (!wait_or_abort<kPolls>(ptx::smem_u32(&bar_kv_empty[slot]), phase ^ 1u, abort_ptr, p.timeout_ns,
                                kRoleProducer)) {
               ok = false;
               break;
@@ -419,7 +431,7 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
         }
         // Once its Q K^T products have completed, the partner may write its
         // partial result over this CTA's Q tiles.
-        if (ok && wait_or_abort(ptx::smem_u32(&bar_q_empty), uc & 1, abort_ptr, p.timeout_ns, kRoleProducer))
+        if (ok && wait_or_abort<kPolls>(ptx::smem_u32(&bar_q_empty), uc & 1, abort_ptr, p.timeout_ns, kRoleProducer))
           ptx::mbar_arrive_remote(ptx::mapa_shared(ptx::smem_u32(&bar_peer_ready), tp.rank ^ 1u));
       }
       if (!ok || *abort_ptr) {
@@ -475,20 +487,20 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
     int g = 0, uc = 0;
     for (int u = blockIdx.x; u < p.num_whole && ok; u += gridDim.x, ++uc) {
       const int it0 = 2 * n_kv * uc;
-      ok = wait_warp_or_abort(ptx::smem_u32(&bar_q_full), uc & 1, abort_ptr, p.timeout_ns, kRoleMma);
+      ok = wait_warp_or_abort<kPolls>(ptx::smem_u32(&bar_q_full), uc & 1, abort_ptr, p.timeout_ns, kRoleMma);
       if (ok)
-        ok = wait_warp_or_abort(ptx::smem_u32(&bar_kv_full[it0 % C::kStages]), (it0 / C::kStages) & 1, abort_ptr,
+        ok = wait_warp_or_abort<kPolls>(ptx::smem_u32(&bar_kv_full[it0 % C::kStages]), (it0 / C::kStages) & 1, abort_ptr,
                                 p.timeout_ns, kRoleMma);
       for (int j = 0; j < n_kv && ok; ++j, ++g) {
         const int itK = it0 + 2 * j;
         ptx::tc_fence_after();
         for (int t = 0; t < 2 && ok; ++t) {
           if (j > 0) {
-            ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_half[t]), (g - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
+            ok = wait_warp_or_abort<kPolls>(ptx::smem_u32(&bar_p_half[t]), (g - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
             if (!ok) break;
             ptx::tc_fence_after();
             issue_pv_half(t, itK - 1, j > 1, 0);
-            ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_full[t]), (g - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
+            ok = wait_warp_or_abort<kPolls>(ptx::smem_u32(&bar_p_full[t]), (g - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
             if (!ok) break;
             ptx::tc_fence_after();
             issue_pv_half(t, itK - 1, true, 1);
@@ -506,11 +518,11 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
       // The last key block's P V.
       const int itV = it0 + 2 * n_kv - 1;
       for (int t = 0; t < 2 && ok; ++t) {
-        ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_half[t]), (g - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
+        ok = wait_warp_or_abort<kPolls>(ptx::smem_u32(&bar_p_half[t]), (g - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
         if (!ok) break;
         ptx::tc_fence_after();
         issue_pv_half(t, itV, n_kv > 1, 0);
-        ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_full[t]), (g - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
+        ok = wait_warp_or_abort<kPolls>(ptx::smem_u32(&bar_p_full[t]), (g - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
         if (!ok) break;
         ptx::tc_fence_after();
         issue_pv_half(t, itV, true, 1);
@@ -522,20 +534,20 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
       // The split unit: the same sequence over this CTA's half of the key blocks.
       const int it0 = 2 * n_kv * uc;
       const int nb = tp.kb1 - tp.kb0;
-      ok = wait_warp_or_abort(ptx::smem_u32(&bar_q_full), uc & 1, abort_ptr, p.timeout_ns, kRoleMma);
+      ok = wait_warp_or_abort<kPolls>(ptx::smem_u32(&bar_q_full), uc & 1, abort_ptr, p.timeout_ns, kRoleMma);
       if (ok)
-        ok = wait_warp_or_abort(ptx::smem_u32(&bar_kv_full[it0 % C::kStages]), (it0 / C::kStages) & 1, abort_ptr,
+        ok = wait_warp_or_abort<kPolls>(ptx::smem_u32(&bar_kv_full[it0 % C::kStages]), (it0 / C::kStages) & 1, abort_ptr,
                                 p.timeout_ns, kRoleMma);
       for (int j = 0; j < nb && ok; ++j, ++g) {
         const int itK = it0 + 2 * j;
         ptx::tc_fence_after();
         for (int t = 0; t < 2 && ok; ++t) {
           if (j > 0) {
-            ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_half[t]), (g - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
+            ok = wait_warp_or_abort<kPolls>(ptx::smem_u32(&bar_p_half[t]), (g - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
             if (!ok) break;
             ptx::tc_fence_after();
             issue_pv_half(t, itK - 1, j > 1, 0);
-            ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_full[t]), (g - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
+            ok = wait_warp_or_abort<kPolls>(ptx::smem_u32(&bar_p_full[t]), (g - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
             if (!ok) break;
             ptx::tc_fence_after();
             issue_pv_half(t, itK - 1, true, 1);
@@ -551,11 +563,11 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
       }
       const int itV = it0 + 2 * nb - 1;
       for (int t = 0; t < 2 && ok; ++t) {
-        ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_half[t]), (g - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
+        ok = wait_warp_or_abort<kPolls>(ptx::smem_u32(&bar_p_half[t]), (g - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
         if (!ok) break;
         ptx::tc_fence_after();
         issue_pv_half(t, itV, nb > 1, 0);
-        ok = wait_warp_or_abort(ptx::smem_u32(&bar_p_full[t]), (g - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
+        ok = wait_warp_or_abort<kPolls>(ptx::smem_u32(&bar_p_full[t]), (g - 1) & 1, abort_ptr, p.timeout_ns, kRoleMma);
         if (!ok) break;
         ptx::tc_fence_after();
         issue_pv_half(t, itV, true, 1);
@@ -591,14 +603,14 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
       // the MMA issuer); waiting here costs nothing, S_t(j) comes later.
       {
         const int itV = it0 + 2 * j + 1;
-        ok = wait_warp_or_abort(ptx::smem_u32(&bar_kv_full[itV % C::kStages]), (itV / C::kStages) & 1, abort_ptr,
+        ok = wait_warp_or_abort<kPolls>(ptx::smem_u32(&bar_kv_full[itV % C::kStages]), (itV / C::kStages) & 1, abort_ptr,
                                 p.timeout_ns, kRoleSoftmax);
         if (ok && j + 1 < n_kv)
-          ok = wait_warp_or_abort(ptx::smem_u32(&bar_kv_full[(itV + 1) % C::kStages]), ((itV + 1) / C::kStages) & 1,
+          ok = wait_warp_or_abort<kPolls>(ptx::smem_u32(&bar_kv_full[(itV + 1) % C::kStages]), ((itV + 1) / C::kStages) & 1,
                                   abort_ptr, p.timeout_ns, kRoleSoftmax);
         if (!ok) break;
       }
-      ok = wait_warp_or_abort(ptx::smem_u32(&bar_s_full[t]), g & 1, abort_ptr, p.timeout_ns, kRoleSoftmax);
+      ok = wait_warp_or_abort<kPolls>(ptx::smem_u32(&bar_s_full[t]), g & 1, abort_ptr, p.timeout_ns, kRoleSoftmax);
       if (!ok) break;
       ptx::tc_fence_after();
       // The loads also reduce each 32-column piece to its maximum, which is
@@ -806,7 +818,7 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
       ptx::tc_fence_before();
       ptx::mbar_arrive(ptx::smem_u32(&bar_p_full[t]));
     }
-    if (ok) ok = wait_warp_or_abort(ptx::smem_u32(&bar_o_full[t]), uc & 1, abort_ptr, p.timeout_ns, kRoleSoftmax);
+    if (ok) ok = wait_warp_or_abort<kPolls>(ptx::smem_u32(&bar_o_full[t]), uc & 1, abort_ptr, p.timeout_ns, kRoleSoftmax);
     if (ok) {
       ptx::tc_fence_after();
       const int bh = unit_head(u);
@@ -868,14 +880,14 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
         // the MMA issuer); waiting here costs nothing, S_t(j) comes later.
         {
           const int itV = it0 + 2 * (j - tp.kb0) + 1;
-          ok = wait_warp_or_abort(ptx::smem_u32(&bar_kv_full[itV % C::kStages]), (itV / C::kStages) & 1, abort_ptr,
+          ok = wait_warp_or_abort<kPolls>(ptx::smem_u32(&bar_kv_full[itV % C::kStages]), (itV / C::kStages) & 1, abort_ptr,
                                   p.timeout_ns, kRoleSoftmax);
           if (ok && j + 1 < tp.kb1)
-            ok = wait_warp_or_abort(ptx::smem_u32(&bar_kv_full[(itV + 1) % C::kStages]), ((itV + 1) / C::kStages) & 1,
+            ok = wait_warp_or_abort<kPolls>(ptx::smem_u32(&bar_kv_full[(itV + 1) % C::kStages]), ((itV + 1) / C::kStages) & 1,
                                     abort_ptr, p.timeout_ns, kRoleSoftmax);
           if (!ok) break;
         }
-        ok = wait_warp_or_abort(ptx::smem_u32(&bar_s_full[t]), g & 1, abort_ptr, p.timeout_ns, kRoleSoftmax);
+        ok = wait_warp_or_abort<kPolls>(ptx::smem_u32(&bar_s_full[t]), g & 1, abort_ptr, p.timeout_ns, kRoleSoftmax);
         if (!ok) break;
         ptx::tc_fence_after();
         // The loads also reduce each 32-column piece to its maximum, which is
@@ -1008,7 +1020,7 @@ __global__ void __launch_bounds__(FwdCfg<HD>::kThreads, 1)
         ptx::tc_fence_before();
         ptx::mbar_arrive(ptx::smem_u32(&bar_p_full[t]));
       }
-      if (ok) ok = wait_warp_or_abort(ptx::smem_u32(&bar_o_full[t]), uc & 1, abort_ptr, p.timeout_ns, kRoleSoftmax);
+      if (ok) ok = wait_warp_or_abort<kPolls>(ptx::smem_u32(&bar_o_full[t]), uc & 1, abort_ptr, p.timeout_ns, kRoleSoftmax);
       const int bh = unit_head(tp.u);
       const int grow = unit_row0(tp.u) + t * C::kBM + row;
       if (ok && t != static_cast<int>(tp.rank)) {
